@@ -1,0 +1,150 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+Shared by the tests, the smoke check and the benchmark, on both sides of a
+parity check (the fp64 oracle and the CUDA library).  This module only draws
+random numbers and lays them out: it holds none of the attention arithmetic.
+
+Every tensor is drawn on the CPU from ``torch.Generator().manual_seed(seed)``
+in fp32 and rounded to bf16, in the fixed order q, k, v, dO, then extras, so
+both sides see the same bf16 bits.
+
+Workloads (sizes and value distributions as the pages give them):
+
+* ``causal_small``   B=1, H=1, S=256, D=64, causal, dO = ones
+  (flash-dmattn PR #122, "Problem": seed 42, loss = out.sum()).
+* ``low_lse_row``    B=2, H=4, D=64/128, (Sq, Sk) in {392x392, 360x64,
+  100x77, 392x512}, bool / additive / no key-padding mask hiding the last
+  ceil(0.1 Sk) keys; every key gets 36 u added (u a random unit vector) and
+  one query row is -36 u, so that row's LSE sits far below -88.7
+  (OpenWAM PR #64, "Validation": one query row anti-aligned with keys that
+  share a large component).
+* ``wide_spread``    B=2, S=8192, H=32, D=128, k = N(0,1) * s for s in
+  {8, 16, 24, 32, 48, 64} (FlyDSL PR #1033, "Repro").
+* ``varlen_gqa``     16 packed sequences, lengths uniform in [128, 4096],
+  Hq=32, Hkv=8, D=128, causal, 512 trailing rows that belong to no sequence.
+* ``long_seq``       B=1, H=16, D=128, S in {16384, 65536, 131072}.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+BF16 = torch.bfloat16
+
+
+def _gen(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+def _randn(g, shape):
+    return torch.randn(*shape, generator=g, dtype=torch.float32)
+
+
+def dense_qkvdo(B, Sq, Sk, Hq, Hkv, D, seed=42, dout="randn", k_scale=1.0):
+    """q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D], dO like q; bf16 on the CPU."""
+    g = _gen(seed)
+    q = _randn(g, (B, Sq, Hq, D)).to(BF16)
+    k = (_randn(g, (B, Sk, Hkv, D)) * k_scale).to(BF16)
+    v = _randn(g, (B, Sk, Hkv, D)).to(BF16)
+    if dout == "ones":
+        do = torch.ones(B, Sq, Hq, D, dtype=BF16)
+    else:
+        do = _randn(g, (B, Sq, Hq, D)).to(BF16)
+    return q, k, v, do
+
+
+def causal_small(seed=42):
+    """B=1, Hq=Hkv=1, S=256, D=64, causal, dO = ones."""
+    q, k, v, do = dense_qkvdo(1, 256, 256, 1, 1, 64, seed=seed, dout="ones")
+    return dict(q=q, k=k, v=v, do=do, causal=True, scale=1.0 / 8.0, mask=None)
+
+
+def padding_mask(B, Sq, Sk, kind, Hq=1, per_row=False, seed=7):
+    """Key-padding mask that hides the last ceil(0.1 Sk) keys.
+
+    kind: "bool" (uint8 1 = visible), "additive" (fp32 0 / -inf) or "none".
+    Shape [B,1,1,Sk] expanded (stride 0) to [B,Hq,Sq,Sk]; with per_row=True a
+    materialised [B,Hq,Sq,Sk] mask that additionally hides random keys.
+    """
+    if kind == "none":
+        return None
+    n_hidden = math.ceil(0.1 * Sk)
+    vis = torch.ones(B, 1, 1, Sk, dtype=torch.bool)
+    if n_hidden:
+        vis[..., Sk - n_hidden:] = False
+    if per_row:
+        g = _gen(seed)
+        extra = torch.rand(B, Hq, Sq, Sk, generator=g) < 0.2
+        vis = vis.expand(B, Hq, Sq, Sk) & ~extra
+        vis = vis.contiguous()
+    else:
+        vis = vis.expand(B, Hq, Sq, Sk)
+    if kind == "bool":
+        return vis.to(torch.uint8) if not per_row else vis.to(torch.uint8)
+    add = torch.zeros(vis.shape, dtype=torch.float32)
+    add = add.masked_fill(~vis, float("-inf"))
+    if not per_row:
+        add = add[:, :1, :1, :].expand(B, Hq, Sq, Sk)
+    return add
+
+
+def low_lse_row(Sq, Sk, mask_kind, D=128, row="first", seed=42, B=2, H=4):
+    """Keys share 36 u; one query row is -36 u (row LSE far below -88.7)."""
+    g = _gen(seed)
+    q = _randn(g, (B, Sq, H, D))
+    k = _randn(g, (B, Sk, H, D))
+    v = _randn(g, (B, Sk, H, D))
+    do = _randn(g, (B, Sq, H, D))
+    u = _randn(g, (D,))
+    u = u / u.norm()
+    k = k + 36.0 * u
+    r = 0 if row == "first" else Sq - 1
+    q[:, r, :, :] = -36.0 * u
+    mask = padding_mask(B, Sq, Sk, mask_kind, Hq=H)
+    return dict(q=q.to(BF16), k=k.to(BF16), v=v.to(BF16), do=do.to(BF16),
+                causal=False, scale=1.0 / math.sqrt(D), mask=mask, low_row=r)
+
+
+def wide_spread(s, B=2, S=8192, H=32, D=128, seed=42):
+    """q, v ~ N(0,1); k = bf16(N(0,1) * s); dO ~ N(0,1); non-causal."""
+    q, k, v, do = dense_qkvdo(B, S, S, H, H, D, seed=seed, k_scale=float(s))
+    return dict(q=q, k=k, v=v, do=do, causal=False, scale=1.0 / math.sqrt(D), mask=None)
+
+
+def varlen_lengths(n=16, lo=128, hi=4096, seed=42):
+    g = _gen(seed)
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
+
+
+def varlen_gqa(n=16, lo=128, hi=4096, Hq=32, Hkv=8, D=128, trailing=512, seed=42):
+    """Packed THD: q/dO [T,Hq,D], k/v [T,Hkv,D], cu_seqlens int32 [n+1]."""
+    lens = varlen_lengths(n, lo, hi, seed)
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    T = cu[-1] + trailing
+    g = _gen(seed + 1)
+    q = _randn(g, (T, Hq, D)).to(BF16)
+    k = _randn(g, (T, Hkv, D)).to(BF16)
+    v = _randn(g, (T, Hkv, D)).to(BF16)
+    do = _randn(g, (T, Hq, D)).to(BF16)
+    return dict(q=q, k=k, v=v, do=do, cu_seqlens=torch.tensor(cu, dtype=torch.int32),
+                max_seqlen=max(lens), causal=True, scale=1.0 / math.sqrt(D), lens=lens)
+
+
+def long_seq(S, causal, B=1, H=16, D=128, seed=42):
+    q, k, v, do = dense_qkvdo(B, S, S, H, H, D, seed=seed)
+    return dict(q=q, k=k, v=v, do=do, causal=causal, scale=1.0 / math.sqrt(D), mask=None)
+
+
+def sample_rows(B, H, S, n=64, seed=5):
+    """n seeded query rows per (b, h), always including 0 and S-1."""
+    g = _gen(seed)
+    rows = []
+    for b in range(B):
+        for h in range(H):
+            idx = torch.randperm(S, generator=g)[: max(n - 2, 0)].tolist()
+            pick = sorted(set([0, S - 1] + idx))[:n]
+            rows += [(b, h, i) for i in pick]
+    return rows

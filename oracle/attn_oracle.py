@@ -1,0 +1,234 @@
+"""fp64 CPU oracle for scaled-dot-product attention, forward and backward.
+
+TEST INFRASTRUCTURE, NOT PART OF THE LIBRARY.  Only the test-suite, the smoke
+check of ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import
+this module.  It shares no code with the CUDA path: it computes the plain
+definition, one (batch, head) at a time, with numpy fp64 matrix products.
+
+What it computes (the definition that every page relies on):
+
+* scores   s_ij = scale * q_i . k_j + bias_ij, where bias is the user's
+  additive mask, -inf for a bool mask entry that is False, -inf for a causal
+  pair j > i (top-left alignment), and keys outside a sequence do not exist.
+  Sources: flash-dmattn PR #122, "Problem" (causal call with ``scale=None``);
+  OpenWAM PR #64, "Summary" and "Fix" (bool mask False = hidden, additive
+  -inf = hidden, zero keys hidden in the mask get exactly zero attention).
+* forward  P = softmax_j(s), out = P v, lse_i = m_i + log sum_j exp(s_ij - m_i)
+  in natural log (OpenWAM PR #64, "Summary": the row log-sum-exp and
+  exp(0 - lse)).  The oracle takes the exact row max m_i once; the GPU's
+  online max / lazy rescale (FlyDSL PR #1033, "Root cause" and "The fix")
+  must reach the same numbers.
+* a row with no visible key (m_i = -inf) has out_i = 0 and lse_i = 0, and it
+  contributes no gradient.  The pages do not define this row; 0 rather than
+  -inf follows the reasoning of PFCCLab/cudnn-frontend PR #9, section 2
+  (a -inf statistic turns into -inf - (-inf) = NaN downstream).
+* backward (the standard analytic gradient of out = softmax(s) v with
+  upstream gradient dO):
+      dP = dO v^T,  Delta_i = sum_j P_ij dP_ij (= rowsum(dO * out)),
+      dS = P * (dP - Delta),  dQ = scale dS K,  dK = scale dS^T Q,
+      dV = P^T dO;
+  with grouped-query attention (GQA) dK and dV of a kv head are summed over
+  the q heads that share it (flash-dmattn PR #122 names num_heads and
+  num_kv_heads).
+* varlen packed sequences: rows [cu[s], cu[s+1]) form sequence s; rows past
+  cu[-1] belong to no sequence and come back as out = 0, lse = 0 and zero
+  gradients (PFCCLab/cudnn-frontend PR #9, section 2: rows the scheduler
+  never visits must still be written).
+
+Layouts follow the library: q/out/dout [B, Sq, Hq, D]; k/v [B, Sk, Hkv, D];
+lse [B, Hq, Sq]; varlen q [T, Hq, D], k/v [T, Hkv, D], lse [Hq, T].
+Masks are broadcastable to [B, Hq, Sq, Sk]: a bool array (True = visible) or a
+float array (additive).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "attn_fwd",
+    "attn_bwd",
+    "attn_varlen",
+    "attn_rows",
+    "bias_for",
+]
+
+
+def _as64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def bias_for(mask, b, h, Sq, Sk, causal, rows=None):
+    """Additive fp64 bias for one (batch, q head): [Sq, Sk], or [len(rows), Sk].
+
+    bool mask: True = visible (0), False = hidden (-inf).  Float mask: added
+    as is.  Causal: key j > query i is hidden (top-left alignment).
+    ``rows`` selects query rows (default: all Sq of them).
+    """
+    ri = np.arange(Sq) if rows is None else np.asarray(rows)
+    bias = np.zeros((len(ri), Sk), dtype=np.float64)
+    if mask is not None:
+        m = np.asarray(mask)
+        while m.ndim < 4:
+            m = m[None]
+        mb = m[b if m.shape[0] > 1 else 0, h if m.shape[1] > 1 else 0]
+        mb = np.broadcast_to(mb, (Sq, Sk))[ri]
+        if mb.dtype == np.bool_:
+            bias = np.where(mb, 0.0, -np.inf)
+        else:
+            bias = bias + mb.astype(np.float64)
+    if causal:
+        j = np.arange(Sk)[None, :]
+        bias = np.where(j > ri[:, None], -np.inf, bias)
+    return bias
+
+
+def _fwd_head(qh, kh, vh, bias, scale):
+    """One (batch, head): returns P [Sq,Sk], out [Sq,D], lse [Sq].
+
+    Softmax over the scores with the exact row max; rows with no visible key
+    give P = 0, out = 0, lse = 0.
+    """
+    s = scale * (qh @ kh.T) + bias
+    Sq, Sk = s.shape
+    if Sk == 0:
+        m = np.full(Sq, -np.inf)
+    else:
+        m = s.max(axis=1)
+    live = m > -np.inf
+    m_safe = np.where(live, m, 0.0)
+    e = np.exp(s - m_safe[:, None])          # exp(-inf) = 0 for hidden keys
+    e[~live] = 0.0
+    l = e.sum(axis=1)
+    P = np.zeros_like(e)
+    P[live] = e[live] / l[live, None]
+    out = P @ vh
+    lse = np.zeros(Sq)
+    lse[live] = m[live] + np.log(l[live])
+    return P, out, lse
+
+
+def _bwd_head(qh, kh, vh, P, dOh, scale):
+    """Analytic gradients of one (batch, q head) given its P and dO."""
+    dP = dOh @ vh.T
+    delta = (P * dP).sum(axis=1)
+    dS = P * (dP - delta[:, None])
+    dq = scale * (dS @ kh)
+    dk = scale * (dS.T @ qh)
+    dv = P.T @ dOh
+    return dq, dk, dv
+
+
+def _default_scale(D, scale):
+    return 1.0 / math.sqrt(D) if scale is None else float(scale)
+
+
+def attn_fwd(q, k, v, mask=None, causal=False, scale=None):
+    """Dense forward.  q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] -> out, lse [B,Hq,Sq]."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    assert Hq % Hkv == 0
+    G = Hq // Hkv
+    sc = _default_scale(D, scale)
+    out = np.zeros((B, Sq, Hq, v.shape[-1]))
+    lse = np.zeros((B, Hq, Sq))
+    for b in range(B):
+        for h in range(Hq):
+            bias = bias_for(mask, b, h, Sq, Sk, causal)
+            _, o, l = _fwd_head(q[b, :, h], k[b, :, h // G], v[b, :, h // G], bias, sc)
+            out[b, :, h] = o
+            lse[b, h] = l
+    return out, lse
+
+
+def attn_bwd(q, k, v, dout, mask=None, causal=False, scale=None):
+    """Dense forward + backward.  Returns out, lse, dq, dk, dv (fp64)."""
+    q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    assert Hq % Hkv == 0
+    G = Hq // Hkv
+    sc = _default_scale(D, scale)
+    out = np.zeros_like(q)
+    lse = np.zeros((B, Hq, Sq))
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            bias = bias_for(mask, b, h, Sq, Sk, causal)
+            P, o, l = _fwd_head(q[b, :, h], k[b, :, hk], v[b, :, hk], bias, sc)
+            out[b, :, h] = o
+            lse[b, h] = l
+            gq, gk, gv = _bwd_head(q[b, :, h], k[b, :, hk], v[b, :, hk], P, dout[b, :, h], sc)
+            dq[b, :, h] = gq
+            dk[b, :, hk] += gk
+            dv[b, :, hk] += gv
+    return out, lse, dq, dk, dv
+
+
+def attn_varlen(q, k, v, dout, cu_seqlens, causal=False, scale=None, heads=None):
+    """Packed varlen (THD) forward + backward.
+
+    q/dout [T,Hq,D], k/v [T,Hkv,D]; sequence s owns rows [cu[s], cu[s+1]) of
+    all four, so Sq = Sk per sequence.  Rows >= cu[-1] get zeros everywhere.
+    ``heads`` optionally restricts the work to a subset of q heads (their
+    kv heads' dK/dV then hold only those q heads' contributions).
+    Returns out, lse [Hq,T], dq, dk, dv.
+    """
+    q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    sc = _default_scale(D, scale)
+    cu = [int(x) for x in cu_seqlens]
+    out = np.zeros_like(q)
+    lse = np.zeros((Hq, T))
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    hs = range(Hq) if heads is None else heads
+    for s in range(len(cu) - 1):
+        a, e = cu[s], cu[s + 1]
+        L = e - a
+        if L == 0:
+            continue
+        for h in hs:
+            hk = h // G
+            bias = bias_for(None, 0, 0, L, L, causal)
+            P, o, l = _fwd_head(q[a:e, h], k[a:e, hk], v[a:e, hk], bias, sc)
+            out[a:e, h] = o
+            lse[h, a:e] = l
+            gq, gk, gv = _bwd_head(q[a:e, h], k[a:e, hk], v[a:e, hk], P, dout[a:e, h], sc)
+            dq[a:e, h] = gq
+            dk[a:e, hk] += gk
+            dv[a:e, hk] += gv
+    return out, lse, dq, dk, dv
+
+
+def attn_rows(q, k, v, dout, rows, mask=None, causal=False, scale=None):
+    """Selected query rows of a dense problem, each computed on its own.
+
+    ``rows`` is a list of (b, h, i).  For each, returns out_i [D], lse_i and
+    dq_i [D]; dq_i needs only row i's P, dP and Delta, so the cost is
+    O(Sk * D) per row.
+    """
+    q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    sc = _default_scale(D, scale)
+    outs, lses, dqs = [], [], []
+    for (b, h, i) in rows:
+        hk = h // G
+        bias = bias_for(mask, b, h, Sq, Sk, causal, rows=[i])
+        P, o, l = _fwd_head(q[b, i:i + 1, h], k[b, :, hk], v[b, :, hk], bias, sc)
+        gq, _, _ = _bwd_head(q[b, i:i + 1, h], k[b, :, hk], v[b, :, hk], P,
+                             dout[b, i:i + 1, h], sc)
+        outs.append(o[0])
+        lses.append(l[0])
+        dqs.append(gq[0])
+    return np.array(outs), np.array(lses), np.array(dqs)
