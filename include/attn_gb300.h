@@ -1,0 +1,191 @@
+/*
+ * attn_gb300.h - C ABI of the fused scaled-dot-product attention library
+ * (forward and backward) for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (the formula every source page assumes; see "Sources" below):
+ *
+ *   s_ij  = scale * q_i . k_j + mask_ij            (mask: additive, or a bool
+ *                                                    mask with False = -inf;
+ *                                                    causal hides j > i)
+ *   out_i = sum_j softmax_j(s_i)_j v_j
+ *   lse_i = log sum_j exp(s_ij)                      (natural log, fp32)
+ *
+ *   backward, given dO = d(loss)/d(out):
+ *   Delta_i = sum_d dO_id out_id,  P = softmax(s),  dP = dO V^T,
+ *   dS = P o (dP - Delta),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+ *
+ * Sources (the web pages this library follows):
+ *   - flash-dmattn PR #122 "Fix NaN/Inf values in dV gradients", Problem and
+ *     Root Cause: the causal B=1,H=1,S=256,D=64 bf16 call, and the rule that
+ *     gradient accumulators must be zero-initialised (never empty_like).
+ *   - ROCm/FlyDSL PR #1033 "Fix NaN from the lazy rescale on a wide score
+ *     range", Root cause / The fix: the online softmax must take
+ *     m_new = max(m_row, m_tile) before it rescales.
+ *   - NVIDIA/cudnn-frontend PR #429 "Fix stream-ordering and input-validation
+ *     holes in the SM100 DSA backward interface": every allocation and
+ *     zero-fill goes on the launch stream; the dtype gate must match the
+ *     kernel; companion tensors are checked against the shape contract; all
+ *     inputs on one device; strided out-parameters are rejected.
+ *   - PFCCLab/cudnn-frontend PR #9 "DSA: fix dK SMEM handoff race ...",
+ *     sections 1-4: barrier-protected staging before a bulk store, rows the
+ *     scheduler never visits are written (0, not -inf), the exp2 exponent is
+ *     clamped, unsupported head_dim is rejected.
+ *   - OpenWAM PR #64, Summary / Fix: the last partial key tile must be
+ *     predicated in the backward too, or a row whose lse is below -88.7
+ *     evaluates exp(0 - lse) = inf there.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *   Tensors are described by attn_tensor_t: a device pointer, an element type,
+ *   a rank, a shape and strides counted in ELEMENTS.  The library never
+ *   allocates and never frees; the caller owns every buffer.  All work
+ *   (zero-fills included) is enqueued on the caller's `stream`; nothing runs
+ *   on the legacy default stream, and the calls do not synchronise.
+ *
+ *   Layouts
+ *     dense  : q, out, dout [B, Sq, Hq, D]; k, v [B, Sk, Hkv, D];
+ *              lse [B, Hq, Sq] fp32; mask broadcastable to [B, Hq, Sq, Sk].
+ *     varlen : q, out, dout [T, Hq, D]; k, v [T, Hkv, D]; lse [Hq, T];
+ *              cu_seqlens int32 [nseq + 1] on the device, cu[0] = 0,
+ *              non-decreasing, cu[nseq] <= T.  Sequence s owns rows
+ *              [cu[s], cu[s+1]) of q, k and v (so Sq = Sk per sequence).
+ *              Rows >= cu[nseq] belong to no sequence; the library writes
+ *              them as out = 0, lse = 0, dq = dk = dv = 0.
+ *   Inputs q, k, v, dout, out (as a backward input): bf16, last-dim stride 1,
+ *   every other stride a multiple of 8 elements (16 bytes), base 16-byte
+ *   aligned.  Outputs out, lse, dq, dk, dv: contiguous in the layouts above.
+ *   Head dim D must be 64 or 128; Hq must be a multiple of Hkv (GQA).
+ *   Causal masking is top-left aligned: key j is hidden from query i when
+ *   j > i.  A query row with no visible key gets out = 0, lse = 0 and a zero
+ *   dq row; keys that no query sees get zero dk and dv.
+ *
+ *   Inputs must be finite.  Values in rows outside a sequence (varlen) may be
+ *   read by a partial tile and are multiplied by exact zeros.
+ *
+ *   Errors: every entry point returns ATTN_OK (0) or a negative ATTN_E_*
+ *   code.  A validation failure launches nothing.  Faults found on the device
+ *   (a malformed cu_seqlens, a bounded wait that ran out) are recorded in a
+ *   per-device error word and the affected tiles are skipped; read and clear
+ *   it with attn_get_error().
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st* attn_stream_t;
+
+/* Element types. */
+enum {
+    ATTN_BF16 = 1,
+    ATTN_F16 = 2,   /* recognised so that it can be rejected: not computed */
+    ATTN_F32 = 3,
+    ATTN_I32 = 4,
+    ATTN_U8 = 5     /* bool mask: nonzero = visible, 0 = hidden */
+};
+
+/* Return codes. */
+enum {
+    ATTN_OK = 0,
+    ATTN_E_DTYPE = -1,        /* element type not supported for this argument */
+    ATTN_E_SHAPE = -2,        /* shape breaks the contract derived from q      */
+    ATTN_E_LAYOUT = -3,       /* stride / alignment / contiguity violation     */
+    ATTN_E_DEVICE = -4,       /* tensors on different devices, or host memory  */
+    ATTN_E_UNSUPPORTED = -5,  /* head dim, mask+varlen, ... not implemented    */
+    ATTN_E_WORKSPACE = -6,    /* workspace missing, too small or misaligned    */
+    ATTN_E_CUDA = -7,         /* a CUDA runtime call failed                    */
+    ATTN_E_TIMEOUT = -8,      /* device: a bounded wait gave up                */
+    ATTN_E_SEQLENS = -9,      /* device: cu_seqlens malformed / over max_seqlen*/
+    ATTN_E_ARG = -10          /* null pointer or non-finite scale              */
+};
+
+/* Flags (bitwise OR). */
+enum {
+    ATTN_DETERMINISTIC = 1u,  /* backward: dQ by a separate kernel, no atomics;
+                                 dq, dk, dv are bitwise reproducible */
+    ATTN_EAGER_RESCALE = 2u   /* forward: rescale the running output on every
+                                 new row max (disables the lazy threshold) */
+};
+
+typedef struct {
+    void* data;          /* device pointer */
+    int32_t dtype;       /* ATTN_BF16, ATTN_F32, ATTN_I32, ATTN_U8, ... */
+    int32_t ndim;        /* 1 .. 4 */
+    int64_t shape[4];
+    int64_t stride[4];   /* in elements; 0 = broadcast (masks only) */
+    int32_t device;      /* CUDA device ordinal, or -1 for host memory */
+} attn_tensor_t;
+
+/*
+ * attn_fwd - forward pass: out and lse.
+ *
+ *   q, k, v     bf16 inputs (dense [B,S,H,D] or varlen [T,H,D]).
+ *   mask        NULL, or a dense-only mask broadcastable to [B,Hq,Sq,Sk]
+ *               (rank 4, stride 0 on broadcast axes): ATTN_U8 (bool,
+ *               0 = hidden), ATTN_F32 or ATTN_BF16 (additive, -inf = hidden).
+ *               The mask is added after scaling.
+ *   cu_seqlens  NULL for dense, else int32 [nseq+1] on the device (varlen).
+ *   max_seqlen  varlen only: an upper bound on every sequence length (a
+ *               longer sequence is skipped and flagged ATTN_E_SEQLENS).
+ *   causal      nonzero = causal (top-left).
+ *   scale       finite softmax scale (callers usually pass 1/sqrt(D)).
+ *   out         bf16, same shape as q, contiguous; fully written.
+ *   lse         fp32 [B,Hq,Sq] (dense) or [Hq,T] (varlen), contiguous; fully
+ *               written, natural log.
+ *   flags       0 or ATTN_EAGER_RESCALE.
+ *   stream      every launch and zero-fill is enqueued here.
+ */
+int attn_fwd(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t* v,
+             const attn_tensor_t* mask, const attn_tensor_t* cu_seqlens, int32_t max_seqlen,
+             int causal, float scale, attn_tensor_t* out, attn_tensor_t* lse,
+             uint32_t flags, attn_stream_t stream);
+
+/*
+ * attn_bwd_workspace_bytes - size of the scratch buffer attn_bwd needs for
+ * this q / k / flags combination (fp32 dQ accumulator and the per-row
+ * Delta and log2-domain lse vectors).  Returns 0 if q or k is malformed.
+ */
+size_t attn_bwd_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* k, uint32_t flags);
+
+/*
+ * attn_bwd - backward pass: dq, dk, dv.
+ *
+ *   q, k, v, out, dout, lse   as produced / consumed by attn_fwd with the
+ *               same mask, cu_seqlens, max_seqlen, causal and scale.
+ *   dq, dk, dv  bf16, shapes of q, k, v, contiguous; fully written (the
+ *               caller may pass uninitialised memory).
+ *   workspace   device buffer of at least attn_bwd_workspace_bytes() bytes,
+ *               256-byte aligned; contents on entry are ignored (it is
+ *               zero-filled on `stream`) and are undefined on return.
+ *   flags       0 or ATTN_DETERMINISTIC.
+ */
+int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t* v,
+             const attn_tensor_t* out, const attn_tensor_t* dout, const attn_tensor_t* lse,
+             const attn_tensor_t* mask, const attn_tensor_t* cu_seqlens, int32_t max_seqlen,
+             int causal, float scale, attn_tensor_t* dq, attn_tensor_t* dk, attn_tensor_t* dv,
+             void* workspace, size_t workspace_bytes, uint32_t flags, attn_stream_t stream);
+
+/*
+ * attn_get_error - synchronises `stream`, then returns and clears the error
+ * word of the current device: ATTN_OK, ATTN_E_SEQLENS or ATTN_E_TIMEOUT
+ * (ATTN_E_CUDA if the synchronisation itself failed).
+ */
+int attn_get_error(attn_stream_t stream);
+
+/* attn_strerror - static, human-readable text for a return code. */
+const char* attn_strerror(int code);
+
+/* attn_version - library version as major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -210,25 +210,32 @@ def attn_varlen(q, k, v, dout, cu_seqlens, causal=False, scale=None, heads=None)
 
 
 def attn_rows(q, k, v, dout, rows, mask=None, causal=False, scale=None):
-    """Selected query rows of a dense problem, each computed on its own.
+    """Selected query rows of a dense problem.
 
     ``rows`` is a list of (b, h, i).  For each, returns out_i [D], lse_i and
-    dq_i [D]; dq_i needs only row i's P, dP and Delta, so the cost is
-    O(Sk * D) per row.
+    dq_i [D].  Row i's dq needs only its own P, dP and Delta, so the cost is
+    O(Sk * D) per row; rows of one (b, h) are stacked into one matrix product.
     """
     q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
     B, Sq, Hq, D = q.shape
     Sk, Hkv = k.shape[1], k.shape[2]
     G = Hq // Hkv
     sc = _default_scale(D, scale)
-    outs, lses, dqs = [], [], []
-    for (b, h, i) in rows:
+    n = len(rows)
+    outs = np.zeros((n, v.shape[-1]))
+    lses = np.zeros(n)
+    dqs = np.zeros((n, D))
+    groups = {}
+    for idx, (b, h, i) in enumerate(rows):
+        groups.setdefault((b, h), []).append((idx, i))
+    for (b, h), items in groups.items():
         hk = h // G
-        bias = bias_for(mask, b, h, Sq, Sk, causal, rows=[i])
-        P, o, l = _fwd_head(q[b, i:i + 1, h], k[b, :, hk], v[b, :, hk], bias, sc)
-        gq, _, _ = _bwd_head(q[b, i:i + 1, h], k[b, :, hk], v[b, :, hk], P,
-                             dout[b, i:i + 1, h], sc)
-        outs.append(o[0])
-        lses.append(l[0])
-        dqs.append(gq[0])
-    return np.array(outs), np.array(lses), np.array(dqs)
+        idxs = [t[0] for t in items]
+        ii = [t[1] for t in items]
+        bias = bias_for(mask, b, h, Sq, Sk, causal, rows=ii)
+        P, o, l = _fwd_head(q[b, ii, h], k[b, :, hk], v[b, :, hk], bias, sc)
+        gq, _, _ = _bwd_head(q[b, ii, h], k[b, :, hk], v[b, :, hk], P, dout[b, ii, h], sc)
+        outs[idxs] = o
+        lses[idxs] = l
+        dqs[idxs] = gq
+    return outs, lses, dqs

@@ -1,0 +1,8 @@
+"""Fused scaled-dot-product attention (forward and backward) for GB300.
+
+The compute lives in a CUDA library built for sm_103a (``build.build()``)
+behind the C ABI of ``include/attn_gb300.h``; this package is its binding.
+"""
+from .ops import attn_bwd, attn_fwd, bwd_workspace_bytes, get_error  # noqa: F401
+
+__all__ = ["attn_fwd", "attn_bwd", "bwd_workspace_bytes", "get_error"]

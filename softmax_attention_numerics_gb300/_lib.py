@@ -1,0 +1,83 @@
+"""ctypes view of the C ABI in include/attn_gb300.h (no torch types)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+ATTN_BF16, ATTN_F16, ATTN_F32, ATTN_I32, ATTN_U8 = 1, 2, 3, 4, 5
+ATTN_DETERMINISTIC = 1
+ATTN_EAGER_RESCALE = 2
+
+ERRORS = {
+    0: "ATTN_OK", -1: "ATTN_E_DTYPE", -2: "ATTN_E_SHAPE", -3: "ATTN_E_LAYOUT",
+    -4: "ATTN_E_DEVICE", -5: "ATTN_E_UNSUPPORTED", -6: "ATTN_E_WORKSPACE",
+    -7: "ATTN_E_CUDA", -8: "ATTN_E_TIMEOUT", -9: "ATTN_E_SEQLENS", -10: "ATTN_E_ARG",
+}
+
+# Every symbol the header declares.
+EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_error",
+           "attn_strerror", "attn_version")
+
+
+class AttnTensor(ctypes.Structure):
+    _fields_ = [
+        ("data", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("ndim", ctypes.c_int32),
+        ("shape", ctypes.c_int64 * 4),
+        ("stride", ctypes.c_int64 * 4),
+        ("device", ctypes.c_int32),
+    ]
+
+
+PT = ctypes.POINTER(AttnTensor)
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load the shared library; raise if it has not been built (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "CUDA attention library not built (%s missing); run "
+            "softmax_attention_numerics_gb300.build.build() first" % path)
+    lib = ctypes.CDLL(path)
+    lib.attn_fwd.restype = ctypes.c_int
+    lib.attn_fwd.argtypes = [PT, PT, PT, PT, PT, ctypes.c_int32, ctypes.c_int, ctypes.c_float,
+                             PT, PT, ctypes.c_uint32, ctypes.c_void_p]
+    lib.attn_bwd.restype = ctypes.c_int
+    lib.attn_bwd.argtypes = [PT, PT, PT, PT, PT, PT, PT, PT, ctypes.c_int32, ctypes.c_int,
+                             ctypes.c_float, PT, PT, PT, ctypes.c_void_p, ctypes.c_size_t,
+                             ctypes.c_uint32, ctypes.c_void_p]
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_bwd_workspace_bytes.argtypes = [PT, PT, ctypes.c_uint32]
+    lib.attn_get_error.restype = ctypes.c_int
+    lib.attn_get_error.argtypes = [ctypes.c_void_p]
+    lib.attn_strerror.restype = ctypes.c_char_p
+    lib.attn_strerror.argtypes = [ctypes.c_int]
+    lib.attn_version.restype = ctypes.c_int
+    lib.attn_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        text = load().attn_strerror(code).decode()
+        super().__init__("%s failed: %s (%s)" % (where, ERRORS.get(code, code), text))
+
+
+def check(code: int, where: str):
+    if code != 0:
+        raise AttnError(code, where)

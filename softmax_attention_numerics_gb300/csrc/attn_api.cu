@@ -1,0 +1,425 @@
+// Host side of the C ABI declared in include/attn_gb300.h: argument
+// validation (before any launch), problem set-up and the launch sequence on
+// the caller's stream.
+//
+// The checks follow NVIDIA/cudnn-frontend PR #429 ("Fix stream-ordering and
+// input-validation holes ..."): every companion tensor is checked against
+// the shape contract derived from q (a transposed dout or lse must fail, not
+// run), all tensors sit on one device, the dtype gate matches what the
+// kernels compute (bf16 only; fp16 is rejected, never reinterpreted), and
+// out-parameters must be contiguous.  Unsupported head dims are rejected
+// before launch (PFCCLab/cudnn-frontend PR #9, section 4).
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+
+#include "../../include/attn_gb300.h"
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+// Device error word (one per device that loads the library).
+__device__ int g_attn_error = 0;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {nullptr};
+std::mutex g_err_mu;
+
+int* error_word(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_attn_error) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(ptr);
+    }
+    return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// bf16 input: rank r, last stride 1, other strides multiples of 8 elements
+// (for dims longer than 1), 16-byte aligned base.
+int check_input(const attn_tensor_t* t, int rank) {
+    if (!t) return ATTN_E_ARG;
+    if (t->dtype != ATTN_BF16) return ATTN_E_DTYPE;
+    if (t->ndim != rank) return ATTN_E_SHAPE;
+    int64_t n = 1;
+    for (int i = 0; i < rank; ++i) {
+        if (t->shape[i] < 0) return ATTN_E_SHAPE;
+        n *= t->shape[i];
+    }
+    if (n > 0 && !t->data) return ATTN_E_ARG;
+    if (t->stride[rank - 1] != 1) return ATTN_E_LAYOUT;
+    for (int i = 0; i < rank - 1; ++i)
+        if (t->shape[i] > 1 && (t->stride[i] <= 0 || (t->stride[i] % 8) != 0)) return ATTN_E_LAYOUT;
+    if (!aligned16(t->data)) return ATTN_E_LAYOUT;
+    return ATTN_OK;
+}
+
+bool is_contiguous(const attn_tensor_t* t) {
+    int64_t s = 1;
+    for (int i = t->ndim - 1; i >= 0; --i) {
+        if (t->shape[i] != 1 && t->stride[i] != s) return false;
+        s *= t->shape[i];
+    }
+    return true;
+}
+
+bool same_shape(const attn_tensor_t* t, const int64_t* shape, int rank) {
+    if (t->ndim != rank) return false;
+    for (int i = 0; i < rank; ++i)
+        if (t->shape[i] != shape[i]) return false;
+    return true;
+}
+
+int check_output(const attn_tensor_t* t, int dtype, const int64_t* shape, int rank) {
+    if (!t) return ATTN_E_ARG;
+    if (t->dtype != dtype) return ATTN_E_DTYPE;
+    if (!same_shape(t, shape, rank)) return ATTN_E_SHAPE;
+    int64_t n = 1;
+    for (int i = 0; i < rank; ++i) n *= shape[i];
+    if (n > 0 && !t->data) return ATTN_E_ARG;
+    if (!is_contiguous(t)) return ATTN_E_LAYOUT;
+    if (n > 0 && !aligned16(t->data)) return ATTN_E_LAYOUT;
+    return ATTN_OK;
+}
+
+int check_device(const attn_tensor_t* t, int dev) {
+    if (!t) return ATTN_OK;
+    if (t->device < 0) return ATTN_E_DEVICE;
+    if (t->device != dev) return ATTN_E_DEVICE;
+    return ATTN_OK;
+}
+
+#define ATTN_TRY(x)                       \
+    do {                                  \
+        const int _rc = (x);              \
+        if (_rc != ATTN_OK) return _rc;   \
+    } while (0)
+
+// Shape contract derived from q and k; fills the shape-related fields of p.
+struct Shapes {
+    int varlen;
+    int64_t B, Sq, Sk, Hq, Hkv, D, T, nseq;
+    int64_t q_shape[4], k_shape[4], lse_shape[3];
+    int rank, lse_rank;
+};
+
+int derive_shapes(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t* v,
+                  const attn_tensor_t* cu, int32_t max_seqlen, Shapes* s) {
+    s->varlen = cu != nullptr;
+    s->rank = s->varlen ? 3 : 4;
+    if (!q || !k || !v) return ATTN_E_ARG;
+    if (q->dtype == ATTN_F16 || k->dtype == ATTN_F16 || v->dtype == ATTN_F16) return ATTN_E_DTYPE;
+    if (q->ndim == s->rank && q->shape[s->rank - 1] != 64 && q->shape[s->rank - 1] != 128)
+        return ATTN_E_UNSUPPORTED;
+    ATTN_TRY(check_input(q, s->rank));
+    ATTN_TRY(check_input(k, s->rank));
+    ATTN_TRY(check_input(v, s->rank));
+    if (s->varlen) {
+        s->T = q->shape[0];
+        s->Hq = q->shape[1];
+        s->D = q->shape[2];
+        s->Hkv = k->shape[1];
+        if (k->shape[0] != s->T || k->shape[2] != s->D) return ATTN_E_SHAPE;
+        if (!same_shape(v, k->shape, 3)) return ATTN_E_SHAPE;
+        if (cu->dtype != ATTN_I32) return ATTN_E_DTYPE;
+        if (cu->ndim != 1 || cu->shape[0] < 1) return ATTN_E_SHAPE;
+        if (cu->stride[0] != 1 && cu->shape[0] > 1) return ATTN_E_LAYOUT;
+        if (!cu->data) return ATTN_E_ARG;
+        if (max_seqlen < 0) return ATTN_E_ARG;
+        s->nseq = cu->shape[0] - 1;
+        s->B = s->nseq;
+        s->Sq = s->Sk = max_seqlen;
+        const int64_t qs[3] = {s->T, s->Hq, s->D};
+        const int64_t ks[3] = {s->T, s->Hkv, s->D};
+        for (int i = 0; i < 3; ++i) {
+            s->q_shape[i] = qs[i];
+            s->k_shape[i] = ks[i];
+        }
+        s->lse_rank = 2;
+        s->lse_shape[0] = s->Hq;
+        s->lse_shape[1] = s->T;
+    } else {
+        s->B = q->shape[0];
+        s->Sq = q->shape[1];
+        s->Hq = q->shape[2];
+        s->D = q->shape[3];
+        s->Sk = k->shape[1];
+        s->Hkv = k->shape[2];
+        s->T = 0;
+        if (k->shape[0] != s->B || k->shape[3] != s->D) return ATTN_E_SHAPE;
+        if (!same_shape(v, k->shape, 4)) return ATTN_E_SHAPE;
+        for (int i = 0; i < 4; ++i) {
+            s->q_shape[i] = q->shape[i];
+            s->k_shape[i] = k->shape[i];
+        }
+        s->lse_rank = 3;
+        s->lse_shape[0] = s->B;
+        s->lse_shape[1] = s->Hq;
+        s->lse_shape[2] = s->Sq;
+    }
+    if (s->D != 64 && s->D != 128) return ATTN_E_UNSUPPORTED;
+    if (s->Hkv <= 0 || s->Hq <= 0 || s->Hq % s->Hkv != 0) return ATTN_E_SHAPE;
+    if (s->Sq > INT32_MAX / 2 || s->Sk > INT32_MAX / 2 || s->T > INT32_MAX / 2 ||
+        s->B > 65535 || s->Hq > 65535)
+        return ATTN_E_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+void strides_in(const attn_tensor_t* t, int varlen, int64_t* xb, int64_t* xs, int64_t* xh) {
+    if (varlen) {
+        *xb = 0;
+        *xs = t->stride[0];
+        *xh = t->stride[1];
+    } else {
+        *xb = t->stride[0];
+        *xs = t->stride[1];
+        *xh = t->stride[2];
+    }
+}
+
+int fill_common(Problem* p, const Shapes& s, const attn_tensor_t* q, const attn_tensor_t* k,
+                const attn_tensor_t* v, const attn_tensor_t* mask, const attn_tensor_t* cu,
+                int causal, float scale, uint32_t flags) {
+    *p = Problem();
+    p->q = static_cast<const bf16*>(q->data);
+    p->k = static_cast<const bf16*>(k->data);
+    p->v = static_cast<const bf16*>(v->data);
+    strides_in(q, s.varlen, &p->q_b, &p->q_s, &p->q_h);
+    strides_in(k, s.varlen, &p->k_b, &p->k_s, &p->k_h);
+    strides_in(v, s.varlen, &p->v_b, &p->v_s, &p->v_h);
+    p->B = static_cast<int>(s.B);
+    p->Hq = static_cast<int>(s.Hq);
+    p->Hkv = static_cast<int>(s.Hkv);
+    p->G = static_cast<int>(s.Hq / s.Hkv);
+    p->Sq = static_cast<int>(s.Sq);
+    p->Sk = static_cast<int>(s.Sk);
+    p->D = static_cast<int>(s.D);
+    p->varlen = s.varlen;
+    p->cu = s.varlen ? static_cast<const int*>(cu->data) : nullptr;
+    p->T = static_cast<int>(s.T);
+    if (s.varlen) {
+        p->out_b = 0;
+        p->out_s = s.Hq * s.D;
+        p->out_h = s.D;
+        p->dk_b = 0;
+        p->dk_s = s.Hkv * s.D;
+        p->dk_h = s.D;
+        p->lse_b = 0;
+        p->lse_h = s.T;
+        p->acc_b = 0;
+    } else {
+        p->out_b = s.Sq * s.Hq * s.D;
+        p->out_s = s.Hq * s.D;
+        p->out_h = s.D;
+        p->dk_b = s.Sk * s.Hkv * s.D;
+        p->dk_s = s.Hkv * s.D;
+        p->dk_h = s.D;
+        p->lse_b = s.Hq * s.Sq;
+        p->lse_h = s.Sq;
+        p->acc_b = s.Sq;
+    }
+    p->mask_kind = MASK_NONE;
+    if (mask) {
+        if (s.varlen) return ATTN_E_UNSUPPORTED;
+        if (!mask->data) return ATTN_E_ARG;
+        if (mask->ndim != 4) return ATTN_E_SHAPE;
+        const int64_t full[4] = {s.B, s.Hq, s.Sq, s.Sk};
+        int64_t st[4];
+        for (int i = 0; i < 4; ++i) {
+            if (mask->shape[i] != full[i] && mask->shape[i] != 1) return ATTN_E_SHAPE;
+            st[i] = mask->shape[i] == 1 ? 0 : mask->stride[i];
+            if (st[i] < 0) return ATTN_E_LAYOUT;
+        }
+        if (mask->dtype == ATTN_U8)
+            p->mask_kind = MASK_BOOL;
+        else if (mask->dtype == ATTN_F32)
+            p->mask_kind = MASK_F32;
+        else if (mask->dtype == ATTN_BF16)
+            p->mask_kind = MASK_BF16;
+        else
+            return ATTN_E_DTYPE;
+        p->mask = mask->data;
+        p->m_b = st[0];
+        p->m_h = st[1];
+        p->m_q = st[2];
+        p->m_k = st[3];
+    }
+    if (!isfinite(scale)) return ATTN_E_ARG;
+    p->causal = causal ? 1 : 0;
+    p->scale = scale;
+    p->scale_log2 = scale * 1.4426950408889634f;
+    p->lazy = (flags & ATTN_EAGER_RESCALE) ? 0 : 1;
+    return ATTN_OK;
+}
+
+int current_device(int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return ATTN_E_CUDA;
+    return ATTN_OK;
+}
+
+// Device checks and the error word; runs after every host-only check.
+int bind_device(Problem* p, std::initializer_list<const attn_tensor_t*> ts) {
+    int dev;
+    ATTN_TRY(current_device(&dev));
+    for (const attn_tensor_t* t : ts) ATTN_TRY(check_device(t, dev));
+    p->err = error_word(dev);
+    return p->err ? ATTN_OK : ATTN_E_CUDA;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+    size_t acc, delta, lse2, total;
+};
+
+WsLayout ws_layout(const Shapes& s, uint32_t flags) {
+    const int64_t rows = s.varlen ? s.T : s.B * s.Sq;
+    WsLayout w;
+    const size_t acc_bytes =
+        (flags & ATTN_DETERMINISTIC) ? 0 : round256(static_cast<size_t>(rows * s.Hq * s.D) * 4);
+    const size_t vec_bytes = round256(static_cast<size_t>(rows * s.Hq) * 4);
+    w.acc = 0;
+    w.delta = acc_bytes;
+    w.lse2 = w.delta + vec_bytes;
+    w.total = w.lse2 + vec_bytes;
+    return w;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_E_CUDA; }
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t* v,
+                        const attn_tensor_t* mask, const attn_tensor_t* cu_seqlens,
+                        int32_t max_seqlen, int causal, float scale, attn_tensor_t* out,
+                        attn_tensor_t* lse, uint32_t flags, attn_stream_t stream) {
+    Shapes s;
+    ATTN_TRY(derive_shapes(q, k, v, cu_seqlens, max_seqlen, &s));
+    ATTN_TRY(check_output(out, ATTN_BF16, s.q_shape, s.rank));
+    ATTN_TRY(check_output(lse, ATTN_F32, s.lse_shape, s.lse_rank));
+    Problem p;
+    ATTN_TRY(fill_common(&p, s, q, k, v, mask, cu_seqlens, causal, scale, flags));
+    ATTN_TRY(bind_device(&p, {q, k, v, mask, cu_seqlens, out, lse}));
+    p.out = static_cast<bf16*>(out->data);
+    p.lse = static_cast<float*>(lse->data);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (s.varlen) ATTN_TRY(cuda_rc(launch_zero_trailing_fwd(p, st)));
+    return cuda_rc(launch_fwd(p, st));
+}
+
+extern "C" size_t attn_bwd_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* k,
+                                           uint32_t flags) {
+    if (!q || !k) return 0;
+    Shapes s;
+    s.varlen = q->ndim == 3;
+    if (s.varlen) {
+        s.T = q->shape[0];
+        s.Hq = q->shape[1];
+        s.D = q->shape[2];
+        s.B = 0;
+        s.Sq = 0;
+    } else if (q->ndim == 4) {
+        s.B = q->shape[0];
+        s.Sq = q->shape[1];
+        s.Hq = q->shape[2];
+        s.D = q->shape[3];
+        s.T = 0;
+    } else {
+        return 0;
+    }
+    if (s.D != 64 && s.D != 128) return 0;
+    return ws_layout(s, flags).total;
+}
+
+extern "C" int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t* v,
+                        const attn_tensor_t* out, const attn_tensor_t* dout,
+                        const attn_tensor_t* lse, const attn_tensor_t* mask,
+                        const attn_tensor_t* cu_seqlens, int32_t max_seqlen, int causal,
+                        float scale, attn_tensor_t* dq, attn_tensor_t* dk, attn_tensor_t* dv,
+                        void* workspace, size_t workspace_bytes, uint32_t flags,
+                        attn_stream_t stream) {
+    Shapes s;
+    ATTN_TRY(derive_shapes(q, k, v, cu_seqlens, max_seqlen, &s));
+    if (!out || !dout || !lse) return ATTN_E_ARG;
+    if (out->dtype == ATTN_F16 || dout->dtype == ATTN_F16) return ATTN_E_DTYPE;
+    ATTN_TRY(check_input(out, s.rank));
+    ATTN_TRY(check_input(dout, s.rank));
+    if (!same_shape(out, s.q_shape, s.rank) || !same_shape(dout, s.q_shape, s.rank))
+        return ATTN_E_SHAPE;
+    if (lse->dtype != ATTN_F32) return ATTN_E_DTYPE;
+    if (!same_shape(lse, s.lse_shape, s.lse_rank)) return ATTN_E_SHAPE;
+    if (!is_contiguous(lse)) return ATTN_E_LAYOUT;
+    ATTN_TRY(check_output(dq, ATTN_BF16, s.q_shape, s.rank));
+    ATTN_TRY(check_output(dk, ATTN_BF16, s.k_shape, s.rank));
+    ATTN_TRY(check_output(dv, ATTN_BF16, s.k_shape, s.rank));
+    const WsLayout w = ws_layout(s, flags);
+    if (w.total > 0) {
+        if (!workspace) return ATTN_E_WORKSPACE;
+        if (workspace_bytes < w.total) return ATTN_E_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_E_WORKSPACE;
+    }
+    Problem p;
+    ATTN_TRY(fill_common(&p, s, q, k, v, mask, cu_seqlens, causal, scale, flags));
+    ATTN_TRY(bind_device(&p, {q, k, v, out, dout, lse, mask, cu_seqlens, dq, dk, dv}));
+    p.o = static_cast<const bf16*>(out->data);
+    strides_in(out, s.varlen, &p.o_b, &p.o_s, &p.o_h);
+    p.dout = static_cast<const bf16*>(dout->data);
+    strides_in(dout, s.varlen, &p.do_b, &p.do_s, &p.do_h);
+    p.lse = static_cast<float*>(lse->data);
+    p.dq = static_cast<bf16*>(dq->data);
+    p.dk = static_cast<bf16*>(dk->data);
+    p.dv = static_cast<bf16*>(dv->data);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const bool det = (flags & ATTN_DETERMINISTIC) != 0;
+    p.dq_acc = det ? nullptr : reinterpret_cast<float*>(ws + w.acc);
+    p.delta = reinterpret_cast<float*>(ws + w.delta);
+    p.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!det && w.delta > 0) ATTN_TRY(cuda_rc(cudaMemsetAsync(ws + w.acc, 0, w.delta, st)));
+    ATTN_TRY(cuda_rc(launch_bwd_preprocess(p, st)));
+    if (s.varlen) ATTN_TRY(cuda_rc(launch_zero_trailing_bwd(p, st)));
+    ATTN_TRY(cuda_rc(launch_bwd_main(p, !det, st)));
+    if (det) return cuda_rc(launch_bwd_dq_deterministic(p, st));
+    return cuda_rc(launch_bwd_dq_convert(p, st));
+}
+
+extern "C" int attn_get_error(attn_stream_t stream) {
+    int dev;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_E_CUDA;
+    int* ptr = error_word(dev);
+    if (!ptr) return ATTN_E_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_E_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, ptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_E_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(ptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return ATTN_E_CUDA;
+    return v;
+}
+
+extern "C" const char* attn_strerror(int code) {
+    switch (code) {
+        case ATTN_OK: return "ok";
+        case ATTN_E_DTYPE: return "unsupported element type (bf16 inputs only; fp16 is rejected)";
+        case ATTN_E_SHAPE: return "shape does not match the contract derived from q";
+        case ATTN_E_LAYOUT: return "stride, alignment or contiguity violation";
+        case ATTN_E_DEVICE: return "tensors are not all on the current CUDA device";
+        case ATTN_E_UNSUPPORTED: return "unsupported configuration (head dim must be 64 or 128)";
+        case ATTN_E_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+        case ATTN_E_CUDA: return "a CUDA runtime call failed";
+        case ATTN_E_TIMEOUT: return "a bounded device wait gave up";
+        case ATTN_E_SEQLENS: return "cu_seqlens malformed or a sequence exceeds max_seqlen";
+        case ATTN_E_ARG: return "null pointer or non-finite scale";
+        default: return "unknown error code";
+    }
+}
+
+extern "C" int attn_version(void) { return 100; }

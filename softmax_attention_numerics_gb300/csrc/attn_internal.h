@@ -1,0 +1,75 @@
+// Internal problem description shared by the host entry points and the
+// kernels.  Not part of the public ABI (include/attn_gb300.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+typedef __nv_bfloat16 bf16;
+
+enum MaskKind { MASK_NONE = 0, MASK_BOOL = 1, MASK_F32 = 2, MASK_BF16 = 3 };
+
+// Every stride is in elements.  Row addressing for a (batch b, head h, row i
+// of that batch/sequence) is  ptr + b * x_b + (row0(b) + i) * x_s + h * x_h,
+// where row0(b) = cu[b] for varlen (and x_b = 0) or 0 for dense.
+struct Problem {
+    const bf16* q;
+    const bf16* k;
+    const bf16* v;
+    const bf16* o;      // forward output, read by the backward
+    const bf16* dout;
+    bf16* out;
+    float* lse;
+    bf16* dq;
+    bf16* dk;
+    bf16* dv;
+    float* dq_acc;      // workspace: fp32 [rows, Hq, D]
+    float* delta;       // workspace: fp32, indexed like lse
+    float* lse2;        // workspace: lse * log2(e), indexed like lse
+
+    int64_t q_b, q_s, q_h;
+    int64_t k_b, k_s, k_h;
+    int64_t v_b, v_s, v_h;
+    int64_t o_b, o_s, o_h;
+    int64_t do_b, do_s, do_h;
+    int64_t out_b, out_s, out_h;   // out and dq (contiguous like q)
+    int64_t dk_b, dk_s, dk_h;      // dk and dv (contiguous like k)
+    int64_t lse_b, lse_h;          // lse / delta / lse2: b*lse_b + h*lse_h + row0 + i
+    int64_t acc_b;                 // dq_acc row of (b, i): b*acc_b + row0 + i
+
+    int B;          // batches (dense) or sequences (varlen)
+    int Hq, Hkv, G; // G = Hq / Hkv
+    int Sq, Sk;     // dense lengths; varlen: max_seqlen for both
+    int D;
+    int varlen;
+    const int* cu;  // varlen: int32 [B + 1]
+    int T;          // varlen: total rows of q/k/v
+
+    const void* mask;
+    int mask_kind;
+    int64_t m_b, m_h, m_q, m_k;
+
+    int causal;
+    float scale;
+    float scale_log2;   // scale * log2(e)
+    int lazy;           // 1: lazy rescale with threshold 8 (log2 units)
+    int* err;           // device error word
+};
+
+// Error codes written to the device error word (match include/attn_gb300.h).
+constexpr int DEV_E_TIMEOUT = -8;
+constexpr int DEV_E_SEQLENS = -9;
+
+// Launchers (each enqueues on `stream`, returns cudaGetLastError()).
+cudaError_t launch_fwd(const Problem& p, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const Problem& p, cudaStream_t stream);
+cudaError_t launch_bwd_main(const Problem& p, bool with_dq_atomics, cudaStream_t stream);
+cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq_deterministic(const Problem& p, cudaStream_t stream);
+cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream);
+cudaError_t launch_zero_trailing_bwd(const Problem& p, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,164 @@
+// Memory-bound helper kernels of the backward and the varlen tails:
+//   bwd_preprocess  Delta = rowsum(dO o O) in fp32 and lse2 = lse * log2(e)
+//   dq_convert      dq = bf16(dq_acc * scale)
+//   zero_trailing   rows >= cu[nseq] of a packed varlen buffer: out = 0 and
+//                   lse = 0 (forward), dk = dv = 0 (backward).  Rows that no
+//                   tile visits must still be written (PFCCLab/cudnn-frontend
+//                   PR #9, section 2; flash-dmattn PR #122, Root Cause 1).
+// All are grid-stride loops sized to a multiple of the SM count.
+#include "device_common.cuh"
+
+namespace attn {
+namespace {
+
+// One warp per (row, head); D/32 elements per lane.
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_kernel(const Problem p, int64_t rows) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t total = rows * p.Hq;
+    for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total;
+         w += nwarps) {
+        const int h = static_cast<int>(w % p.Hq);
+        const int64_t r = w / p.Hq;
+        int b;
+        int64_t i;
+        if (p.varlen) {
+            b = 0;
+            i = r;
+        } else {
+            b = static_cast<int>(r / p.Sq);
+            i = r - static_cast<int64_t>(b) * p.Sq;
+        }
+        const bf16* og = p.o + b * p.o_b + i * p.o_s + h * p.o_h;
+        const bf16* dg = p.dout + b * p.do_b + i * p.do_s + h * p.do_h;
+        float acc = 0.f;
+        if (D == 128) {
+            const uint2 ov = *reinterpret_cast<const uint2*>(og + lane * 4);
+            const uint2 dv = *reinterpret_cast<const uint2*>(dg + lane * 4);
+            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+            const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float2 a = __bfloat1622float2(o2[e]);
+                const float2 c = __bfloat1622float2(d2[e]);
+                acc = fmaf(a.x, c.x, acc);
+                acc = fmaf(a.y, c.y, acc);
+            }
+        } else {
+            const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(og + lane * 2);
+            const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(dg + lane * 2);
+            const float2 a = __bfloat1622float2(o2);
+            const float2 c = __bfloat1622float2(d2);
+            acc = fmaf(a.x, c.x, acc);
+            acc = fmaf(a.y, c.y, acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            const int64_t li = b * p.lse_b + h * p.lse_h + i;
+            p.delta[li] = acc;
+            p.lse2[li] = p.lse[li] * kLog2e;
+        }
+    }
+}
+
+// dq = bf16(acc * scale), 4 elements per thread-iteration.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
+                                                         bf16* __restrict__ dq, int64_t n4,
+                                                         float scale) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += stride) {
+        const float4 a = reinterpret_cast<const float4*>(acc)[i];
+        uint2 o;
+        o.x = pack_bf16(a.x * scale, a.y * scale);
+        o.y = pack_bf16(a.z * scale, a.w * scale);
+        reinterpret_cast<uint2*>(dq)[i] = o;
+    }
+}
+
+__device__ __forceinline__ int64_t trailing_start(const Problem& p) {
+    int e = __ldg(p.cu + p.B);
+    if (e < 0) e = 0;
+    if (e > p.T) e = p.T;
+    return e;
+}
+
+// Zero rows [cu[B], T) of a contiguous [T, H, D] bf16 buffer (8 elems per op).
+__device__ __forceinline__ void zero_rows_bf16(bf16* base, int64_t r0, int64_t T, int H, int D) {
+    const int64_t per_row = static_cast<int64_t>(H) * D / 8;
+    const int64_t n = (T - r0) * per_row;
+    uint4* dst = reinterpret_cast<uint4*>(base + r0 * H * D);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += stride)
+        dst[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+__global__ void zero_trailing_fwd_kernel(const Problem p) {
+    const int64_t r0 = trailing_start(p);
+    zero_rows_bf16(p.out, r0, p.T, p.Hq, p.D);
+    const int64_t n = (p.T - r0) * p.Hq;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += stride) {
+        const int64_t h = i / (p.T - r0);
+        const int64_t r = r0 + i % (p.T - r0);
+        p.lse[h * p.lse_h + r] = 0.f;
+    }
+}
+
+__global__ void zero_trailing_bwd_kernel(const Problem p) {
+    const int64_t r0 = trailing_start(p);
+    zero_rows_bf16(p.dk, r0, p.T, p.Hkv, p.D);
+    zero_rows_bf16(p.dv, r0, p.T, p.Hkv, p.D);
+}
+
+int grid_for(int64_t work, int threads) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t blocks = (work + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const Problem& p, cudaStream_t stream) {
+    const int64_t rows = p.varlen ? p.T : static_cast<int64_t>(p.B) * p.Sq;
+    if (rows == 0) return cudaSuccess;
+    const int blocks = grid_for(rows * p.Hq * 32, 256);
+    if (p.D == 64)
+        preprocess_kernel<64><<<blocks, 256, 0, stream>>>(p, rows);
+    else
+        preprocess_kernel<128><<<blocks, 256, 0, stream>>>(p, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream) {
+    const int64_t rows = p.varlen ? p.T : static_cast<int64_t>(p.B) * p.Sq;
+    const int64_t n4 = rows * p.Hq * p.D / 4;
+    if (n4 == 0) return cudaSuccess;
+    dq_convert_kernel<<<grid_for(n4, 256), 256, 0, stream>>>(p.dq_acc, p.dq, n4, p.scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream) {
+    if (!p.varlen || p.T == 0) return cudaSuccess;
+    zero_trailing_fwd_kernel<<<grid_for(static_cast<int64_t>(p.T) * p.Hq * p.D / 8, 256), 256, 0,
+                               stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_trailing_bwd(const Problem& p, cudaStream_t stream) {
+    if (!p.varlen || p.T == 0) return cudaSuccess;
+    zero_trailing_bwd_kernel<<<grid_for(static_cast<int64_t>(p.T) * p.Hkv * p.D / 8, 256), 256,
+                               0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

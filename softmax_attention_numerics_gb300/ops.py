@@ -1,0 +1,130 @@
+"""Python binding of the attention library: argument marshalling only.
+
+Torch is used for device memory and streams.  Every output and the backward
+workspace is allocated inside ``torch.cuda.stream(s)`` for the stream ``s``
+that the library launches on, so allocation, zero-fill and kernels are
+ordered on one stream (NVIDIA/cudnn-frontend PR #429, first fix).  All
+arithmetic runs in the CUDA library; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+
+_DT = {torch.bfloat16: _lib.ATTN_BF16, torch.float16: _lib.ATTN_F16,
+       torch.float32: _lib.ATTN_F32, torch.int32: _lib.ATTN_I32,
+       torch.uint8: _lib.ATTN_U8, torch.bool: _lib.ATTN_U8}
+
+
+def tensor_desc(t):
+    """attn_tensor_t for a torch tensor (or None -> NULL)."""
+    if t is None:
+        return None
+    if t.dim() > 4:
+        raise ValueError("rank > 4 not supported")
+    d = _lib.AttnTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else 0
+    d.dtype = _DT.get(t.dtype, 0)
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    d.device = t.device.index if t.is_cuda else -1
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _stream(stream, device):
+    return stream if stream is not None else torch.cuda.current_stream(device)
+
+
+def _max_seqlen(cu_seqlens, max_seqlen):
+    if cu_seqlens is None:
+        return 0
+    if max_seqlen is None:   # convenience: one device->host read
+        lens = cu_seqlens[1:] - cu_seqlens[:-1]
+        return int(lens.max().item()) if lens.numel() else 0
+    return int(max_seqlen)
+
+
+def attn_fwd(q, k, v, mask=None, cu_seqlens=None, max_seqlen=None, causal=False, scale=None,
+             out=None, lse=None, eager_rescale=False, stream=None):
+    """Forward pass.  Returns (out, lse).
+
+    Dense: q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] -> out like q, lse [B,Hq,Sq] fp32.
+    Varlen (cu_seqlens int32 [n+1]): q [T,Hq,D], k/v [T,Hkv,D], lse [Hq,T].
+    mask: bool (True = visible) or additive fp32/bf16, broadcastable to
+    [B,Hq,Sq,Sk].  scale=None means 1/sqrt(D).
+    """
+    lib = _lib.load()
+    s = _stream(stream, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    msl = _max_seqlen(cu_seqlens, max_seqlen)
+    if mask is not None and mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    with torch.cuda.device(q.device), torch.cuda.stream(s):
+        if out is None:
+            out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+        if lse is None:
+            if cu_seqlens is None:
+                lse = torch.empty(q.shape[0], q.shape[2], q.shape[1], dtype=torch.float32,
+                                  device=q.device)
+            else:
+                lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
+        descs = [tensor_desc(x) for x in (q, k, v, mask, cu_seqlens, out, lse)]
+        rc = lib.attn_fwd(*[_ref(d) for d in descs[:5]], msl, 1 if causal else 0, float(scale),
+                          _ref(descs[5]), _ref(descs[6]),
+                          _lib.ATTN_EAGER_RESCALE if eager_rescale else 0,
+                          ctypes.c_void_p(s.cuda_stream))
+    _lib.check(rc, "attn_fwd")
+    return out, lse
+
+
+def bwd_workspace_bytes(q, k, deterministic=False):
+    lib = _lib.load()
+    dq_, dk_ = tensor_desc(q), tensor_desc(k)
+    return int(lib.attn_bwd_workspace_bytes(ctypes.byref(dq_), ctypes.byref(dk_),
+                                            _lib.ATTN_DETERMINISTIC if deterministic else 0))
+
+
+def attn_bwd(q, k, v, out, dout, lse, mask=None, cu_seqlens=None, max_seqlen=None, causal=False,
+             scale=None, deterministic=False, dq=None, dk=None, dv=None, workspace=None,
+             stream=None):
+    """Backward pass.  Returns (dq, dk, dv) in the shapes of q, k, v."""
+    lib = _lib.load()
+    s = _stream(stream, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    msl = _max_seqlen(cu_seqlens, max_seqlen)
+    if mask is not None and mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    flags = _lib.ATTN_DETERMINISTIC if deterministic else 0
+    with torch.cuda.device(q.device), torch.cuda.stream(s):
+        dq = torch.empty(q.shape, dtype=q.dtype, device=q.device) if dq is None else dq
+        dk = torch.empty(k.shape, dtype=k.dtype, device=k.device) if dk is None else dk
+        dv = torch.empty(v.shape, dtype=v.dtype, device=v.device) if dv is None else dv
+        nbytes = bwd_workspace_bytes(q, k, deterministic)
+        if workspace is None or workspace.numel() < nbytes:
+            workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+        descs = [tensor_desc(x) for x in (q, k, v, out, dout, lse, mask, cu_seqlens)]
+        outs = [tensor_desc(x) for x in (dq, dk, dv)]
+        rc = lib.attn_bwd(*[_ref(d) for d in descs], msl, 1 if causal else 0, float(scale),
+                          *[_ref(d) for d in outs], ctypes.c_void_p(workspace.data_ptr()),
+                          workspace.numel(), flags, ctypes.c_void_p(s.cuda_stream))
+    _lib.check(rc, "attn_bwd")
+    return dq, dk, dv
+
+
+def get_error(stream=None):
+    """Synchronise the stream and return-and-clear the device error word."""
+    lib = _lib.load()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return lib.attn_get_error(ctypes.c_void_p(s.cuda_stream))

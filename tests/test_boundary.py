@@ -1,0 +1,216 @@
+"""Host-side tests of the C ABI: the library builds, loads and exports every
+symbol the header declares, and malformed calls are rejected before any
+launch (NVIDIA/cudnn-frontend PR #429: dtype gate, shape contract including a
+transposed dout or lse, contiguous out-parameters; PFCCLab/cudnn-frontend
+PR #9, section 4: unsupported head_dim).  The descriptors here point at fake
+device addresses: every call under test returns before touching the GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from softmax_attention_numerics_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_gb300.h")
+
+E = {v: k for k, v in _lib.ERRORS.items()}
+FAKE = 1 << 20   # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_expected_api():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True).stdout
+    for name in declared_functions():
+        assert re.search(r"\bT %s\b" % name, out), name
+
+
+def test_version_and_strerror(lib):
+    assert lib.attn_version() >= 100
+    for code in _lib.ERRORS:
+        assert lib.attn_strerror(code)
+
+
+def desc(shape, dtype=_lib.ATTN_BF16, stride=None, data=FAKE, device=0):
+    d = _lib.AttnTensor()
+    d.data = data
+    d.dtype = dtype
+    d.ndim = len(shape)
+    if stride is None:
+        stride, s = [], 1
+        for n in reversed(shape):
+            stride.insert(0, s)
+            s *= n
+    for i, n in enumerate(shape):
+        d.shape[i] = n
+        d.stride[i] = stride[i]
+    d.device = device
+    return d
+
+
+def dense(B=2, Sq=100, Sk=77, Hq=4, Hkv=2, D=128):
+    return dict(q=desc([B, Sq, Hq, D]), k=desc([B, Sk, Hkv, D]), v=desc([B, Sk, Hkv, D]),
+                out=desc([B, Sq, Hq, D]), lse=desc([B, Hq, Sq], _lib.ATTN_F32),
+                dout=desc([B, Sq, Hq, D]), dq=desc([B, Sq, Hq, D]), dk=desc([B, Sk, Hkv, D]),
+                dv=desc([B, Sk, Hkv, D]))
+
+
+def R(x):
+    return None if x is None else ctypes.byref(x)
+
+
+def call_fwd(lib, t, mask=None, cu=None, max_seqlen=0, scale=0.1):
+    return lib.attn_fwd(R(t["q"]), R(t["k"]), R(t["v"]), R(mask), R(cu), max_seqlen, 0, scale,
+                        R(t["out"]), R(t["lse"]), 0, None)
+
+
+def call_bwd(lib, t, mask=None, cu=None, max_seqlen=0, ws=FAKE, ws_bytes=1 << 40, flags=0):
+    return lib.attn_bwd(R(t["q"]), R(t["k"]), R(t["v"]), R(t["out"]), R(t["dout"]), R(t["lse"]),
+                        R(mask), R(cu), max_seqlen, 0, 0.1, R(t["dq"]), R(t["dk"]), R(t["dv"]),
+                        ctypes.c_void_p(ws), ws_bytes, flags, None)
+
+
+def test_rejects_fp16(lib):
+    t = dense()
+    t["q"] = desc([2, 100, 4, 128], _lib.ATTN_F16)
+    assert call_fwd(lib, t) == E["ATTN_E_DTYPE"]
+    t = dense()
+    t["dout"] = desc([2, 100, 4, 128], _lib.ATTN_F16)
+    assert call_bwd(lib, t) == E["ATTN_E_DTYPE"]
+
+
+@pytest.mark.parametrize("D", [32, 96, 100, 112, 192, 256])
+def test_rejects_unsupported_head_dim(lib, D):
+    assert call_fwd(lib, dense(D=D)) == E["ATTN_E_UNSUPPORTED"]
+
+
+def test_rejects_bad_gqa_ratio(lib):
+    assert call_fwd(lib, dense(Hq=6, Hkv=4)) == E["ATTN_E_SHAPE"]
+
+
+def test_rejects_mismatched_companions(lib):
+    t = dense()
+    t["v"] = desc([2, 76, 2, 128])
+    assert call_fwd(lib, t) == E["ATTN_E_SHAPE"]
+    t = dense()
+    t["k"] = desc([1, 77, 2, 128]); t["v"] = desc([1, 77, 2, 128])
+    assert call_fwd(lib, t) == E["ATTN_E_SHAPE"]
+
+
+def test_rejects_transposed_dout_and_lse(lib):
+    t = dense(Sq=100, Hq=4)
+    t["dout"] = desc([2, 4, 100, 128])     # BHSD passed where BSHD is expected
+    assert call_bwd(lib, t) == E["ATTN_E_SHAPE"]
+    t = dense(Sq=100, Hq=4)
+    t["lse"] = desc([2, 100, 4], _lib.ATTN_F32)
+    assert call_bwd(lib, t) == E["ATTN_E_SHAPE"]
+    t = dense()
+    t["lse"] = desc([2, 4, 100], _lib.ATTN_BF16)
+    assert call_bwd(lib, t) == E["ATTN_E_DTYPE"]
+
+
+def test_rejects_layout_violations(lib):
+    t = dense()
+    t["q"] = desc([2, 100, 4, 128], stride=[100 * 4 * 128, 4 * 128, 128, 2])
+    assert call_fwd(lib, t) == E["ATTN_E_LAYOUT"]
+    t = dense()
+    t["k"] = desc([2, 77, 2, 128], stride=[77 * 2 * 132, 2 * 132, 132, 1])   # 264-byte rows
+    assert call_fwd(lib, t) == E["ATTN_E_LAYOUT"]
+    t = dense()
+    t["q"] = desc([2, 100, 4, 128], data=FAKE + 8)
+    assert call_fwd(lib, t) == E["ATTN_E_LAYOUT"]
+
+
+def test_strided_inputs_pass_validation(lib):
+    # A BHSD buffer viewed as BSHD is a legal input (OpenWAM PR #64, Tests:
+    # BSHD buffers viewed as BHSD); it reaches the device stage.
+    t = dense()
+    t["q"] = desc([2, 100, 4, 128], stride=[4 * 100 * 128, 128, 100 * 128, 1])
+    rc = call_fwd(lib, t)
+    assert rc in (0, E["ATTN_E_CUDA"], E["ATTN_E_DEVICE"])
+
+
+def test_rejects_strided_out_params(lib):
+    t = dense()
+    t["out"] = desc([2, 100, 4, 128], stride=[4 * 100 * 128, 128, 100 * 128, 1])
+    assert call_fwd(lib, t) == E["ATTN_E_LAYOUT"]
+    t = dense()
+    t["dk"] = desc([2, 77, 2, 128], stride=[77 * 2 * 128, 128, 77 * 128, 1])
+    assert call_bwd(lib, t) == E["ATTN_E_LAYOUT"]
+
+
+def test_rejects_non_finite_scale(lib):
+    assert call_fwd(lib, dense(), scale=float("nan")) == E["ATTN_E_ARG"]
+    assert call_fwd(lib, dense(), scale=float("inf")) == E["ATTN_E_ARG"]
+
+
+def test_mask_contract(lib):
+    bad = desc([2, 4, 100, 76], _lib.ATTN_U8)
+    assert call_fwd(lib, dense(), mask=bad) == E["ATTN_E_SHAPE"]
+    i32 = desc([2, 1, 1, 77], _lib.ATTN_I32)
+    assert call_fwd(lib, dense(), mask=i32) == E["ATTN_E_DTYPE"]
+    three = desc([2, 100, 77], _lib.ATTN_U8)
+    assert call_fwd(lib, dense(), mask=three) == E["ATTN_E_SHAPE"]
+
+
+def varlen(T=1000, Hq=4, Hkv=2, D=64, n=3):
+    return dict(q=desc([T, Hq, D]), k=desc([T, Hkv, D]), v=desc([T, Hkv, D]),
+                out=desc([T, Hq, D]), lse=desc([Hq, T], _lib.ATTN_F32), dout=desc([T, Hq, D]),
+                dq=desc([T, Hq, D]), dk=desc([T, Hkv, D]), dv=desc([T, Hkv, D])), \
+        desc([n + 1], _lib.ATTN_I32)
+
+
+def test_varlen_contract(lib):
+    t, cu = varlen()
+    t["lse"] = desc([1000, 4], _lib.ATTN_F32)
+    assert call_fwd(lib, t, cu=cu, max_seqlen=512) == E["ATTN_E_SHAPE"]
+    t, cu = varlen()
+    cu.dtype = _lib.ATTN_F32
+    assert call_fwd(lib, t, cu=cu, max_seqlen=512) == E["ATTN_E_DTYPE"]
+    t, cu = varlen()
+    mask = desc([1, 1, 1, 512], _lib.ATTN_U8)
+    assert call_fwd(lib, t, mask=mask, cu=cu, max_seqlen=512) == E["ATTN_E_UNSUPPORTED"]
+    t, cu = varlen()
+    t["k"] = desc([999, 2, 64]); t["v"] = desc([999, 2, 64])
+    assert call_fwd(lib, t, cu=cu, max_seqlen=512) == E["ATTN_E_SHAPE"]
+
+
+def test_host_pointers_rejected(lib):
+    t = dense()
+    t["q"] = desc([2, 100, 4, 128], device=-1)
+    rc = call_fwd(lib, t)
+    assert rc in (E["ATTN_E_DEVICE"], E["ATTN_E_CUDA"])
+
+
+def test_workspace_size_and_checks(lib):
+    t = dense(B=2, Sq=100, Hq=4, D=128)
+    n = lib.attn_bwd_workspace_bytes(R(t["q"]), R(t["k"]), 0)
+    acc = -(-2 * 100 * 4 * 128 * 4 // 256) * 256
+    vec = -(-2 * 100 * 4 * 4 // 256) * 256
+    assert n == acc + 2 * vec
+    nd = lib.attn_bwd_workspace_bytes(R(t["q"]), R(t["k"]), _lib.ATTN_DETERMINISTIC)
+    assert nd == 2 * vec
+    assert call_bwd(lib, t, ws_bytes=n - 1) == E["ATTN_E_WORKSPACE"]
+    assert call_bwd(lib, t, ws=0, ws_bytes=n) == E["ATTN_E_WORKSPACE"]
+    assert call_bwd(lib, t, ws=FAKE + 16, ws_bytes=n) == E["ATTN_E_WORKSPACE"]
+    assert lib.attn_bwd_workspace_bytes(R(dense(D=96)["q"]), R(t["k"]), 0) == 0

@@ -1,0 +1,295 @@
+"""GPU parity of the CUDA attention path against the fp64 oracle.
+
+Every case feeds the same seeded bf16 inputs (attn_workloads) to the library
+(through the C ABI) and to the oracle, and checks the acceptance bar in
+parity_utils plus zero NaN/Inf.  Workloads follow the pages:
+flash-dmattn PR #122 (causal S=256 D=64, loss = out.sum()), OpenWAM PR #64
+(partial last key tile with a row whose lse is far below -88.7), FlyDSL
+PR #1033 (wide logit spread), packed varlen with GQA and trailing rows
+(PFCCLab/cudnn-frontend PR #9, section 2), and long sequences.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_workloads as W
+from oracle import attn_oracle as O
+from parity_utils import (assert_finite, compare, gpu_run, nonfinite, oracle_dense,
+                          oracle_mask, rel_l2, to64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built():
+    from softmax_attention_numerics_gb300 import build
+    build.build()
+    yield
+
+
+# ------------------------------------------------------------- causal S=256 D=64
+
+@pytest.mark.parametrize("mode", ["default", "eager", "deterministic"])
+def test_causal_small(mode):
+    case = W.causal_small()
+    res = gpu_run(case, deterministic=mode == "deterministic", eager=mode == "eager")
+    assert_finite(res)
+    compare(res, oracle_dense(case), ctx="causal_small/" + mode)
+
+
+# ------------------------------------------------------------- low-lse row + key padding
+
+SHAPES = [(392, 392), (360, 64), (100, 77), (392, 512)]
+
+
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("row", ["first", "last"])
+@pytest.mark.parametrize("mask", ["bool", "additive", "none"])
+@pytest.mark.parametrize("shape", SHAPES, ids=["%dx%d" % s for s in SHAPES])
+def test_low_lse_row(shape, mask, row, D):
+    Sq, Sk = shape
+    case = W.low_lse_row(Sq, Sk, mask, D=D, row=row)
+    res = gpu_run(case)
+    assert_finite(res)
+    ref = oracle_dense(case)
+    r = case["low_row"]
+    # the case really exercises the failure condition: exp(0 - lse) overflows fp32
+    assert ref["lse"][:, :, r].max() < -88.73
+    compare(res, ref, ctx="low_lse %s %s %s D=%d" % (shape, mask, row, D))
+    if mask != "none":
+        hidden = Sk - math.ceil(0.1 * Sk)
+        assert torch.count_nonzero(res["dk"][:, hidden:]) == 0
+        assert torch.count_nonzero(res["dv"][:, hidden:]) == 0
+
+
+# ------------------------------------------------------------- wide logit spread
+
+@pytest.mark.parametrize("s", [8, 16, 24, 32, 48, 64])
+def test_wide_spread(s):
+    case = W.wide_spread(s)
+    res = gpu_run(case)
+    assert_finite(res)
+    g = torch.Generator().manual_seed(100 + s)
+    pairs = [(int(torch.randint(0, 2, (1,), generator=g)), int(torch.randint(0, 32, (1,), generator=g)))
+             for _ in range(4)]
+    sc = case["scale"]
+    for (b, h) in pairs:
+        qh, kh, vh, dh = (to64(case[n][b, :, h]) for n in ("q", "k", "v", "do"))
+        P, out, lse = O._fwd_head(qh, kh, vh, np.zeros((qh.shape[0], kh.shape[0])), sc)
+        dq, dk, dv = O._bwd_head(qh, kh, vh, P, dh, sc)
+        del P
+        got = {n: res[n][b, :, h] for n in ("out", "dq", "dk", "dv")}
+        got["lse"] = res["lse"][b, h]
+        rep = compare(got, dict(out=out, lse=lse, dq=dq, dk=dk, dv=dv),
+                      ctx="wide s=%d (b=%d,h=%d)" % (s, b, h))
+        print("wide_spread s=%d b=%d h=%d %s" % (s, b, h, rep))
+
+
+# ------------------------------------------------------------- varlen + GQA + trailing rows
+
+def test_varlen_gqa():
+    case = W.varlen_gqa()
+    res = gpu_run(case)
+    assert_finite(res)
+    cu = case["cu_seqlens"].tolist()
+    end = cu[-1]
+    for n in ("out", "dq", "dk", "dv"):
+        assert torch.count_nonzero(res[n][end:]) == 0, n
+    assert torch.count_nonzero(res["lse"][:, end:]) == 0
+    lens = case["lens"]
+    order = sorted(range(len(lens)), key=lambda i: lens[i])
+    pick = [order[0], order[len(order) // 2], order[-1]]
+    heads = [0, 1, 2, 3, 28, 29, 30, 31]          # kv heads 0 and 7, complete groups
+    for sidx in pick:
+        a, e = cu[sidx], cu[sidx + 1]
+        sub = {n: case[n][a:e] for n in ("q", "k", "v", "do")}
+        out, lse, dq, dk, dv = O.attn_varlen(to64(sub["q"]), to64(sub["k"]), to64(sub["v"]),
+                                             to64(sub["do"]), [0, e - a], causal=True,
+                                             scale=case["scale"], heads=heads)
+        got = dict(out=res["out"][a:e, heads], lse=res["lse"][heads, a:e],
+                   dq=res["dq"][a:e, heads], dk=res["dk"][a:e][:, [0, 7]],
+                   dv=res["dv"][a:e][:, [0, 7]])
+        ref = dict(out=out[:, heads], lse=lse[heads], dq=dq[:, heads], dk=dk[:, [0, 7]],
+                   dv=dv[:, [0, 7]])
+        compare(got, ref, ctx="varlen seq %d (len %d)" % (sidx, e - a))
+
+
+# ------------------------------------------------------------- long sequences (sampled)
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("S", [16384, 65536, 131072])
+def test_long_seq(S, causal):
+    case = W.long_seq(S, causal)
+    res = gpu_run(case)
+    assert_finite(res)
+    rows = W.sample_rows(1, 16, S, n=64)
+    out, lse, dq = O.attn_rows(to64(case["q"]), to64(case["k"]), to64(case["v"]),
+                               to64(case["do"]), rows, causal=causal, scale=case["scale"])
+    bi = [r[0] for r in rows]
+    hi = [r[1] for r in rows]
+    ii = [r[2] for r in rows]
+    got = dict(out=res["out"][bi, ii, hi], lse=res["lse"][bi, hi, ii], dq=res["dq"][bi, ii, hi])
+    compare(got, dict(out=out, lse=lse, dq=dq), names=("out", "lse", "dq"),
+            ctx="long S=%d causal=%s" % (S, causal))
+    if S == 16384:
+        h = 5
+        qh, kh, vh, dh = (to64(case[n][0, :, h]) for n in ("q", "k", "v", "do"))
+        bias = O.bias_for(None, 0, 0, S, S, causal)
+        P, _, _ = O._fwd_head(qh, kh, vh, bias, case["scale"])
+        del bias
+        _, dk, dv = O._bwd_head(qh, kh, vh, P, dh, case["scale"])
+        del P
+        compare(dict(dk=res["dk"][0, :, h], dv=res["dv"][0, :, h]), dict(dk=dk, dv=dv),
+                names=("dk", "dv"), ctx="long S=%d dk/dv head %d" % (S, h))
+
+
+# ------------------------------------------------------------- edge cases
+
+EDGE = [
+    # (B, Sq, Sk, Hq, Hkv, D, causal, mask)
+    (1, 1, 1, 1, 1, 64, False, "none"),
+    (1, 129, 65, 2, 1, 64, False, "none"),
+    (2, 129, 129, 4, 2, 128, True, "none"),
+    (1, 300, 700, 8, 2, 128, False, "bool_rows"),
+    (2, 200, 333, 4, 4, 64, False, "additive_random"),
+    (1, 190, 190, 2, 2, 128, False, "bf16_additive"),
+    (1, 100, 260, 2, 1, 128, True, "none"),          # Sq < Sk, top-left causal
+    (1, 260, 100, 2, 1, 64, True, "none"),           # Sq > Sk
+    (1, 64, 0, 2, 1, 64, False, "none"),             # no keys at all
+    (1, 0, 64, 2, 1, 128, False, "none"),            # no queries
+]
+
+
+def _edge_case(B, Sq, Sk, Hq, Hkv, D, causal, mask):
+    q, k, v, do = W.dense_qkvdo(B, Sq, Sk, Hq, Hkv, D, seed=11)
+    m = None
+    if mask == "bool_rows":
+        m = W.padding_mask(B, Sq, Sk, "bool", Hq=Hq, per_row=True)
+        m[0, 1, 5, :] = 0                           # a fully masked row
+    elif mask == "additive_random":
+        g = torch.Generator().manual_seed(3)
+        m = torch.randn(B, 1, Sq, Sk, generator=g) * 2.0
+        m[..., -7:] = float("-inf")
+    elif mask == "bf16_additive":
+        g = torch.Generator().manual_seed(4)
+        m = (torch.randn(1, Hq, 1, Sk, generator=g) * 3.0).to(torch.bfloat16)
+    return dict(q=q, k=k, v=v, do=do, causal=causal, scale=1.0 / math.sqrt(D), mask=m)
+
+
+@pytest.mark.parametrize("cfg", EDGE, ids=[str(c) for c in EDGE])
+def test_edge_cases(cfg):
+    case = _edge_case(*cfg)
+    for det in (False, True):
+        res = gpu_run(case, deterministic=det)
+        assert_finite(res)
+        compare(res, oracle_dense(case), ctx="edge %s det=%s" % (cfg, det))
+
+
+def test_fully_masked_row_is_zero():
+    case = _edge_case(1, 300, 700, 8, 2, 128, False, "bool_rows")
+    res = gpu_run(case)
+    assert torch.count_nonzero(res["out"][0, 5, 1]) == 0
+    assert res["lse"][0, 1, 5].item() == 0.0
+    assert torch.count_nonzero(res["dq"][0, 5, 1]) == 0
+
+
+def test_strided_bhsd_inputs():
+    """BHSD buffers viewed as BSHD (OpenWAM PR #64, Tests: layout preservation)."""
+    B, S, H, D = 2, 200, 4, 128
+    g = torch.Generator().manual_seed(9)
+    base = [torch.randn(B, H, S, D, generator=g).to(torch.bfloat16) for _ in range(4)]
+    case = dict(q=base[0].transpose(1, 2), k=base[1].transpose(1, 2), v=base[2].transpose(1, 2),
+                do=base[3].transpose(1, 2), causal=True, scale=0.1, mask=None)
+    gcase = dict(case)
+    for n in ("q", "k", "v", "do"):
+        gcase[n] = base[["q", "k", "v", "do"].index(n)].cuda().transpose(1, 2)
+    res = gpu_run(gcase)
+    assert_finite(res)
+    compare(res, oracle_dense(case), ctx="strided")
+
+
+def test_varlen_empty_and_short_sequences():
+    lens = [0, 1, 130, 0, 257, 64]
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    T = cu[-1] + 37
+    g = torch.Generator().manual_seed(12)
+    q = torch.randn(T, 4, 64, generator=g).to(torch.bfloat16)
+    k = torch.randn(T, 2, 64, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, 2, 64, generator=g).to(torch.bfloat16)
+    do = torch.randn(T, 4, 64, generator=g).to(torch.bfloat16)
+    for causal in (False, True):
+        case = dict(q=q, k=k, v=v, do=do, cu_seqlens=torch.tensor(cu, dtype=torch.int32),
+                    max_seqlen=max(lens), causal=causal, scale=0.125)
+        res = gpu_run(case)
+        assert_finite(res)
+        out, lse, dq, dk, dv = O.attn_varlen(to64(q), to64(k), to64(v), to64(do), cu,
+                                             causal=causal, scale=0.125)
+        compare(res, dict(out=out, lse=lse, dq=dq, dk=dk, dv=dv), ctx="varlen short")
+
+
+# ------------------------------------------------------------- determinism
+
+def test_deterministic_path_is_bitwise_stable():
+    case = W.varlen_gqa(n=4, lo=300, hi=900)
+    first = gpu_run(case, deterministic=True)
+    for _ in range(7):
+        again = gpu_run(case, deterministic=True)
+        for n in ("dq", "dk", "dv", "out", "lse"):
+            assert torch.equal(first[n], again[n]), n
+
+
+def test_atomic_path_spread_within_fp32_reassociation_bound():
+    """PFCCLab/cudnn-frontend PR #9, How it was verified: a sum of N fp32 terms
+    in any order differs run to run by at most (N-1) 2^-24 sum|t_i|.  dq_acc
+    gets one partial per 128-key tile (N = 4 here), far below one bf16 ulp, so
+    after rounding to bf16 two runs may differ by at most one ulp (2^-7 of
+    the magnitude), and only where the fp32 sum sits on a rounding boundary."""
+    case = W.low_lse_row(392, 512, "bool", D=128)
+    runs = torch.stack([gpu_run(case)["dq"].float() for _ in range(8)])
+    spread = runs.max(0).values - runs.min(0).values
+    mag = runs.abs().max(0).values
+    assert torch.all(spread <= 2.0 ** -7 * mag)
+    assert (spread > 0).float().mean().item() < 0.05
+
+
+# ------------------------------------------------------------- stream discipline
+
+def test_side_stream_with_busy_ambient_stream():
+    """NVIDIA/cudnn-frontend PR #429, first fix: allocations and zero-fills are
+    ordered with the launch stream even while the ambient stream is busy."""
+    case = W.low_lse_row(392, 392, "bool", D=128)
+    ref = gpu_run(case, deterministic=True)
+    dev = {n: (case[n].cuda() if torch.is_tensor(case[n]) else case[n]) for n in case}
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    torch.cuda._sleep(400_000_000)        # keep the ambient stream busy
+    res = gpu_run(dev, deterministic=True, stream=side)
+    side.synchronize()
+    for n in ("out", "lse", "dq", "dk", "dv"):
+        assert torch.equal(res[n], ref[n]), n
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------- device-side errors
+
+def test_malformed_cu_seqlens_sets_error_word():
+    from softmax_attention_numerics_gb300 import attn_fwd, get_error
+    T = 256
+    q = torch.randn(T, 2, 64, device="cuda").to(torch.bfloat16)
+    k = torch.randn(T, 2, 64, device="cuda").to(torch.bfloat16)
+    cu = torch.tensor([0, 100, 50, 300], dtype=torch.int32, device="cuda")   # decreasing, past T
+    assert get_error() == 0
+    out, lse = attn_fwd(q, k, k, cu_seqlens=cu, max_seqlen=128)
+    assert get_error() == -9          # rows of skipped sequences are undefined
+    assert get_error() == 0
+
+
+def test_cpu_tensors_rejected():
+    from softmax_attention_numerics_gb300 import _lib, attn_fwd
+    q = torch.randn(1, 8, 1, 64).to(torch.bfloat16)
+    with pytest.raises((_lib.AttnError, RuntimeError)):
+        attn_fwd(q.cuda(), q, q.cuda())
