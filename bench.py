@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Attention forward+backward throughput on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+attn_fwd (out, lse) then attn_bwd (Delta preprocess, main backward with
+atomic dQ partials, dQ convert) through the library's C ABI.
+
+Default workload: the long-sequence configuration at its largest size,
+B=1, H=16, S=131072, D=128, bf16, non-causal; q, k, v, dO ~ N(0,1) (seeded).
+Every input tensor (512 MiB each) is far larger than the 129 MB L2, so no L2
+flush is needed between steps.
+
+Metric: fwd+bwd TFLOP/s with algorithmic flops 3.5 * 4*B*H*S^2*D (halved when
+causal).  Prints ONE JSON line (rank 0).  `--impl reference` times the fp64
+CPU oracle instead (a bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOP/s (% of GB300 bf16 tensor peak; non-finite count = 0)"
+KERNEL_SOURCES = ("softmax_attention_numerics_gb300/csrc/bwd_mma.cu",
+                  "softmax_attention_numerics_gb300/csrc/device_common.cuh")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seqlen", type=int, default=131072)
+    ap.add_argument("--heads", type=int, default=16)
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-oracle-reps", type=int, default=1, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def fwd_flops(B, H, S, D, causal):
+    f = 4.0 * B * H * S * S * D
+    return f / 2 if causal else f
+
+
+def workload_name(a):
+    return "long_seq B=1 H=%d S=%d D=128 %s fwd+bwd" % (
+        a.heads, a.seqlen, "causal" if a.causal else "non-causal")
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample_rows(S):
+    """Query rows of head 0 used as the bounded CPU sample (~10-30 s of fp64)."""
+    return max(64, min(S, int(512 * (131072 / S))))
+
+
+def run_oracle_sample(a):
+    """Child process: time the fp64 oracle on query rows [0, m) of head 0
+    against all S keys (full forward+backward arithmetic of those rows)."""
+    import numpy as np
+    from oracle import attn_oracle as O
+    S, D, m = a.seqlen, 128, a.cpu_oracle_sample
+    rng = np.random.default_rng(42)
+    q = rng.standard_normal((m, D)).astype(np.float32).astype(np.float64)
+    k = rng.standard_normal((S, D)).astype(np.float32).astype(np.float64)
+    v = rng.standard_normal((S, D)).astype(np.float32).astype(np.float64)
+    do = rng.standard_normal((m, D)).astype(np.float32).astype(np.float64)
+    bias = O.bias_for(None, 0, 0, S, S, a.causal, rows=np.arange(m)) if a.causal else \
+        np.zeros((m, S))
+    times = []
+    for _ in range(a.cpu_oracle_reps):
+        t0 = time.perf_counter()
+        P, out, lse = O._fwd_head(q, k, v, bias, 1.0 / math.sqrt(D))
+        O._bwd_head(q, k, v, P, do, 1.0 / math.sqrt(D))
+        times.append(time.perf_counter() - t0)
+    if a.causal:
+        vis = float(np.isfinite(bias).sum())
+    else:
+        vis = float(m) * S
+    flops = 3.5 * 4.0 * vis * D
+    print(json.dumps({"times": times, "flops": flops, "rows": m}))
+
+
+def cpu_oracle(a, rows, reps):
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(cores)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-oracle-sample", str(rows),
+           "--cpu-oracle-reps", str(reps), "--seqlen", str(a.seqlen)]
+    if a.causal:
+        cmd.append("--causal")
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    res["cores"] = cores
+    return res
+
+
+def cpu_baseline_entry(a, res):
+    t = min(res["times"])
+    return {"value": res["flops"] / t / 1e12, "unit": "TFLOP/s", "cores": res["cores"],
+            "kind": "oracle",
+            "sample": "fp64 numpy oracle, full fwd+bwd arithmetic of query rows 0..%d of one head "
+                      "against all %d keys (%.3g flop in %.2f s)" % (res["rows"] - 1, a.seqlen,
+                                                                   res["flops"], t)}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """Per-launch DRAM bytes from a committed ncu summary, or None when the
+    kernel source has changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("bytes_per_launch_full")
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rows = max(64, oracle_sample_rows(a.seqlen) // 4)
+    res = cpu_oracle(a, rows, a.warmup + a.steps)
+    times = res["times"][a.warmup:]
+    t = sum(times) / len(times)
+    value = res["flops"] / t / 1e12
+    cb = cpu_baseline_entry(a, dict(res, times=times))
+    cb["value"] = value
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_name(a), "B": 1, "H": a.heads, "S": a.seqlen, "D": 128,
+                   "causal": a.causal, "parallelism": "replicas",
+                   "sample": "each step: fp64 oracle on query rows 0..%d of one head" % (rows - 1)},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- our arm
+
+def main():
+    a = parse()
+    if a.cpu_oracle_sample:
+        run_oracle_sample(a)
+        return
+    if a.impl == "reference":
+        run_reference(a)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    # CPU baseline first: the oracle child process runs before this process
+    # touches the GPU heavily (rank 0 at N=1 only).
+    cpu_res = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu_res = cpu_oracle(a, oracle_sample_rows(a.seqlen), 2)
+
+    from softmax_attention_numerics_gb300 import _lib, attn_bwd, attn_fwd
+    from softmax_attention_numerics_gb300 import build as _build
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    lib = _lib.load()
+
+    B, H, S, D = 1, a.heads, a.seqlen, 128
+    scale = 1.0 / math.sqrt(D)
+    g = torch.Generator(device=dev).manual_seed(42 + rank)
+    shape = (B, S, H, D)
+    q, k, v, do = (torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+                   .to(torch.bfloat16) for _ in range(4))
+    stream = torch.cuda.Stream(device=dev)
+    ws = torch.empty(max(1, _bwd_ws(q, k)), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def step(s):
+        attn_fwd(q, k, v, causal=a.causal, scale=scale, out=out, lse=lse, stream=s)
+        attn_bwd(q, k, v, out, do, lse, causal=a.causal, scale=scale, dq=dq, dk=dk, dv=dv,
+                 workspace=ws, stream=s)
+
+    stages = (_lib.ATTN_STAGE_FWD, _lib.ATTN_STAGE_BWD_PREPROCESS, _lib.ATTN_STAGE_BWD_MAIN,
+              _lib.ATTN_STAGE_BWD_DQ)
+    ev = {st: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(a.steps)] for st in stages}
+    with torch.cuda.stream(stream):
+        for st in stages:
+            for e0, e1 in ev[st]:
+                e0.record(stream)
+                e1.record(stream)
+        for _ in range(a.warmup):
+            step(stream)
+    stream.synchronize()
+
+    # Device-timed region.
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = lib.attn_launch_count()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(a.steps):
+                for st in stages:
+                    lib.attn_profile_events(st, ctypes_ptr(ev[st][i][0]), ctypes_ptr(ev[st][i][1]))
+                step(stream)
+            t1.record(stream)
+        for st in stages:
+            lib.attn_profile_events(st, None, None)
+        stream.synchronize()
+    launches = lib.attn_launch_count() - launches0
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+
+    # Non-finite check of the last step's results.
+    nonfinite = sum(int((~torch.isfinite(t.float())).sum()) for t in (out, lse, dq, dk, dv))
+
+    stage_ms = {st: statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev[st]) for st in stages}
+    ff = fwd_flops(B, H, S, D, a.causal)
+    total_flops = 3.5 * ff * a.steps * world
+    value = total_flops / (ms / 1e3) / 1e12
+
+    peaks, peak_kind = measured_peaks()
+    tensor_peak = peaks.get("bf16_tflops_sustained", 1700.0)
+    main_flops = 2.5 * ff
+    main_achieved = main_flops / (stage_ms[_lib.ATTN_STAGE_BWD_MAIN] / 1e3) / 1e12
+    traffic = ncu_traffic("bwd_main")
+    roofline = {"bound": "tensor", "kernel": "bwd_main", "achieved": main_achieved,
+                "peak": tensor_peak, "unit": "TFLOP/s", "frac": main_achieved / tensor_peak,
+                "traffic": traffic,
+                "peak_source": "%s bf16_tflops_sustained" % peak_kind}
+    fwd_tflops = ff / (stage_ms[_lib.ATTN_STAGE_FWD] / 1e3) / 1e12
+    pre_bytes = B * H * S * (4 * D + 12)
+    dq_bytes = B * H * S * D * 6
+    extra = {
+        "fwd_kernel_tflops": fwd_tflops,
+        "fwd_kernel_frac_of_peak": fwd_tflops / tensor_peak,
+        "bwd_main_ms": stage_ms[_lib.ATTN_STAGE_BWD_MAIN],
+        "fwd_ms": stage_ms[_lib.ATTN_STAGE_FWD],
+        "bwd_preprocess_gbs": pre_bytes / (stage_ms[_lib.ATTN_STAGE_BWD_PREPROCESS] / 1e3) / 1e9,
+        "dq_convert_gbs": dq_bytes / (stage_ms[_lib.ATTN_STAGE_BWD_DQ] / 1e3) / 1e9,
+        "hbm_peak_gbs": peaks.get("hbm_gbs"),
+        "nonfinite_outputs": nonfinite,
+    }
+
+    # End-to-end through the public API with host buffers (pinned), copies timed.
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    dq_in = [torch.empty_like(t) for t in (q, k, v, do)]
+
+    def e2e_step(s):
+        for hdst, hsrc in zip(dq_in, host_in):
+            hdst.copy_(hsrc, non_blocking=True)
+        qq, kk, vv, dd = dq_in
+        o, l = attn_fwd(qq, kk, vv, causal=a.causal, scale=scale, out=out, lse=lse, stream=s)
+        attn_bwd(qq, kk, vv, o, dd, l, causal=a.causal, scale=scale, dq=dq, dk=dk, dv=dv,
+                 workspace=ws, stream=s)
+        for hdst, dsrc in zip(host_out, (out, lse, dq, dk, dv)):
+            hdst.copy_(dsrc, non_blocking=True)
+
+    e_steps = max(1, min(a.steps, 5))
+    with torch.cuda.stream(stream):
+        e2e_step(stream)
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(e_steps):
+            e2e_step(stream)
+        c1.record(stream)
+    stream.synchronize()
+    e_ms = c0.elapsed_time(c1)
+    if world > 1:
+        tt = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e_ms = float(tt.item())
+    e2e_value = 3.5 * ff * e_steps * world / (e_ms / 1e3) / 1e12
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms / a.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_name(a), "B": B, "H": H, "S": S, "D": D,
+                       "causal": a.causal, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "no flush: every input tensor (%d MiB) exceeds L2"
+                             % (q.numel() * 2 >> 20),
+                       "frac_of_peak": value / tensor_peak},
+            "roofline": roofline,
+            "cpu_baseline": cpu_baseline_entry(a, cpu_res) if cpu_res else None,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e_steps},
+            "gpu_launches": int(launches),
+            "clocks": clk.summary(),
+            "extra": extra,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _bwd_ws(q, k):
+    from softmax_attention_numerics_gb300 import bwd_workspace_bytes
+    return bwd_workspace_bytes(q, k)
+
+
+def ctypes_ptr(ev):
+    import ctypes
+    return ctypes.c_void_p(ev.cuda_event)
+
+
+if __name__ == "__main__":
+    main()

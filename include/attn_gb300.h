@@ -184,6 +184,28 @@ const char* attn_strerror(int code);
 /* attn_version - library version as major * 10000 + minor * 100 + patch. */
 int attn_version(void);
 
+/*
+ * Profiling hooks (used by the benchmark; no effect on results).
+ *
+ * attn_profile_events - from now on, record the CUDA events `before` and
+ * `after` (cudaEvent_t handles created by the caller, or NULL to stop) on the
+ * launch stream immediately around the kernel of `stage`.  Process-wide
+ * setting; not thread-safe against concurrent attn_fwd / attn_bwd calls.
+ * Returns ATTN_E_ARG for an unknown stage.
+ */
+enum {
+    ATTN_STAGE_FWD = 0,            /* forward kernel                        */
+    ATTN_STAGE_BWD_PREPROCESS = 1, /* Delta = rowsum(dO o out), lse2         */
+    ATTN_STAGE_BWD_MAIN = 2,       /* dK, dV (and atomic dQ partials)        */
+    ATTN_STAGE_BWD_DQ = 3,         /* dQ convert, or the deterministic dQ    */
+    ATTN_STAGE_COUNT = 4
+};
+int attn_profile_events(int stage, void* before, void* after);
+
+/* attn_launch_count - number of kernels this library has launched in this
+ * process (all devices), for launch accounting. */
+unsigned long long attn_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,7 +18,9 @@ ERRORS = {
 
 # Every symbol the header declares.
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_error",
-           "attn_strerror", "attn_version")
+           "attn_strerror", "attn_version", "attn_profile_events", "attn_launch_count")
+
+ATTN_STAGE_FWD, ATTN_STAGE_BWD_PREPROCESS, ATTN_STAGE_BWD_MAIN, ATTN_STAGE_BWD_DQ = 0, 1, 2, 3
 
 
 class AttnTensor(ctypes.Structure):
@@ -67,6 +69,10 @@ def load():
     lib.attn_strerror.argtypes = [ctypes.c_int]
     lib.attn_version.restype = ctypes.c_int
     lib.attn_version.argtypes = []
+    lib.attn_profile_events.restype = ctypes.c_int
+    lib.attn_profile_events.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    lib.attn_launch_count.restype = ctypes.c_ulonglong
+    lib.attn_launch_count.argtypes = []
     _lib = lib
     return lib
 

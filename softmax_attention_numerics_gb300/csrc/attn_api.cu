@@ -9,6 +9,7 @@
 // kernels compute (bf16 only; fp16 is rejected, never reinterpreted), and
 // out-parameters must be contiguous.  Unsupported head dims are rejected
 // before launch (PFCCLab/cudnn-frontend PR #9, section 4).
+#include <atomic>
 #include <math.h>
 #include <mutex>
 #include <stdint.h>
@@ -35,6 +36,22 @@ int* error_word(int dev) {
         g_err_ptr[dev] = static_cast<int*>(ptr);
     }
     return g_err_ptr[dev];
+}
+
+std::atomic<unsigned long long> g_launches{0};
+cudaEvent_t g_prof[ATTN_STAGE_COUNT][2] = {};
+
+// Launch one stage: optional profiling events around it, launch accounting.
+template <class F>
+int run_stage(int stage, cudaStream_t st, F&& launch) {
+    cudaEvent_t a = stage >= 0 ? g_prof[stage][0] : nullptr;
+    cudaEvent_t b = stage >= 0 ? g_prof[stage][1] : nullptr;
+    if (a && cudaEventRecord(a, st) != cudaSuccess) return ATTN_E_CUDA;
+    const cudaError_t e = launch();
+    if (e != cudaSuccess) return ATTN_E_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (b && cudaEventRecord(b, st) != cudaSuccess) return ATTN_E_CUDA;
+    return ATTN_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -310,8 +327,8 @@ extern "C" int attn_fwd(const attn_tensor_t* q, const attn_tensor_t* k, const at
     p.out = static_cast<bf16*>(out->data);
     p.lse = static_cast<float*>(lse->data);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (s.varlen) ATTN_TRY(cuda_rc(launch_zero_trailing_fwd(p, st)));
-    return cuda_rc(launch_fwd(p, st));
+    if (s.varlen) ATTN_TRY(run_stage(-1, st, [&] { return launch_zero_trailing_fwd(p, st); }));
+    return run_stage(ATTN_STAGE_FWD, st, [&] { return launch_fwd(p, st); });
 }
 
 extern "C" size_t attn_bwd_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* k,
@@ -383,11 +400,12 @@ extern "C" int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const at
     p.lse2 = reinterpret_cast<float*>(ws + w.lse2);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (!det && w.delta > 0) ATTN_TRY(cuda_rc(cudaMemsetAsync(ws + w.acc, 0, w.delta, st)));
-    ATTN_TRY(cuda_rc(launch_bwd_preprocess(p, st)));
-    if (s.varlen) ATTN_TRY(cuda_rc(launch_zero_trailing_bwd(p, st)));
-    ATTN_TRY(cuda_rc(launch_bwd_main(p, !det, st)));
-    if (det) return cuda_rc(launch_bwd_dq_deterministic(p, st));
-    return cuda_rc(launch_bwd_dq_convert(p, st));
+    ATTN_TRY(run_stage(ATTN_STAGE_BWD_PREPROCESS, st, [&] { return launch_bwd_preprocess(p, st); }));
+    if (s.varlen) ATTN_TRY(run_stage(-1, st, [&] { return launch_zero_trailing_bwd(p, st); }));
+    ATTN_TRY(run_stage(ATTN_STAGE_BWD_MAIN, st, [&] { return launch_bwd_main(p, !det, st); }));
+    if (det)
+        return run_stage(ATTN_STAGE_BWD_DQ, st, [&] { return launch_bwd_dq_deterministic(p, st); });
+    return run_stage(ATTN_STAGE_BWD_DQ, st, [&] { return launch_bwd_dq_convert(p, st); });
 }
 
 extern "C" int attn_get_error(attn_stream_t stream) {
@@ -423,3 +441,14 @@ extern "C" const char* attn_strerror(int code) {
 }
 
 extern "C" int attn_version(void) { return 100; }
+
+extern "C" int attn_profile_events(int stage, void* before, void* after) {
+    if (stage < 0 || stage >= ATTN_STAGE_COUNT) return ATTN_E_ARG;
+    g_prof[stage][0] = static_cast<cudaEvent_t>(before);
+    g_prof[stage][1] = static_cast<cudaEvent_t>(after);
+    return ATTN_OK;
+}
+
+extern "C" unsigned long long attn_launch_count(void) {
+    return g_launches.load(std::memory_order_relaxed);
+}

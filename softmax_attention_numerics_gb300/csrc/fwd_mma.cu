@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(kThreads) fwd_mma_kernel(const Problem p) {
             float pv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                pv[e] = bf16_round(ex2(fminf(s[n][e] - msafe[e >> 1], kLazyTau)));
-                l[e >> 1] += pv[e];
+                pv[e] = ex2(fminf(s[n][e] - msafe[e >> 1], kLazyTau));
+                l[e >> 1] += pv[e];      // unrounded: l also feeds the lse
             }
             pf[n >> 1][(n & 1) * 2 + 0] = pack_bf16(pv[0], pv[1]);
             pf[n >> 1][(n & 1) * 2 + 1] = pack_bf16(pv[2], pv[3]);

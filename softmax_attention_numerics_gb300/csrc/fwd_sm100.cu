@@ -1,0 +1,445 @@
+// Attention forward for sm_103a: TMA + tcgen05 (UMMA) + TMEM, warp-specialised.
+//
+// One CTA = two 128-row query tiles (256 rows) of one (batch/sequence, q head).
+//   warps 0-3   softmax for query tile 0 (thread = query row = TMEM lane)
+//   warps 4-7   softmax for query tile 1
+//   warp  8     TMA producer: Q tiles once, then K_j, V_j through a ring
+//   warp  9     TMEM allocator and single-thread UMMA issuer
+// TMEM (512 columns): S0 | S1 (128 fp32 columns each; the bf16 P of a tile is
+// written over the upper half of its S) | O0 | O1 (D columns each).
+//
+// Per key tile j the issuer runs, for t = 0, 1:
+//     O_t += P_t(j) V_j      (P from TMEM, V from shared memory)
+//     S_t  = Q_t K_{j+1}^T   (after O_t's MMA has completed: P_t(j) and
+//                             S_t(j+1) share TMEM columns)
+// so the softmax of one query tile overlaps the MMAs of the other.
+//
+// Softmax (one thread per row, exp2 domain): x = s*scale*log2e (+ mask, with
+// the predicates for the partial last key tile, causal pairs and rows past
+// the sequence), m_tile = max_j x, and ALWAYS m_new = max(m_ref, m_tile)
+// (FlyDSL PR #1033, The fix).  The lazy rule keeps the old reference max
+// while m_tile - m_ref <= 8 and otherwise rescales O_t and l by
+// exp2(m_ref - m_new) in TMEM; rows of the same warp that did not ask for a
+// rescale use a factor of exactly 1.  p = exp2(min(x - m_ref, 8)): the clamp
+// never fires on correct statistics (PFCCLab/cudnn-frontend PR #9, section 3).
+// Epilogue: out = O/l, lse = (m_ref + log2 l) ln 2; l = 0 gives out = 0,
+// lse = 0.  Rows past the sequence are never stored (varlen neighbours).
+#include "sm100_ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace sm100;
+
+constexpr int kFwdThreads = 320;
+constexpr int kTile = 128;
+
+template <int D>
+struct FwdLayout {
+    static constexpr int kBlocks = D / 64;                  // 128-byte column blocks
+    static constexpr int kTileBytes = kTile * D * 2;        // one 128-row bf16 tile
+    static constexpr int kStages = (D == 128) ? 3 : 6;      // K/V ring depth
+    static constexpr int kQ = 0;                            // Q0, Q1
+    static constexpr int kKV = 2 * kTileBytes;
+    static constexpr int kBar = kKV + kStages * kTileBytes;
+    // barrier slots (8 bytes each)
+    static constexpr int kBarQ = 0;
+    static constexpr int kBarKVFull = 1;
+    static constexpr int kBarKVEmpty = kBarKVFull + kStages;
+    static constexpr int kBarSFull = kBarKVEmpty + kStages;   // [2]
+    static constexpr int kBarPFull = kBarSFull + 2;           // [2]
+    static constexpr int kBarPVDone = kBarPFull + 2;          // [2]
+    static constexpr int kBarDrain = kBarPVDone + 2;
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kMisc = kBar + kNumBars * 8;         // tmem base, abort flag
+    static constexpr int kBytes = kMisc + 16 + 1024;          // + alignment slack
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+};
+
+struct FwdMaps {
+    CUtensorMap q, k, v;
+};
+
+template <int D>
+__global__ void __maxnreg__(200)
+    fwd_sm100_kernel(const Problem p, const __grid_constant__ FwdMaps maps) {
+    using L = FwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms.
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + L::kBar + 8u * i; };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int m0 = (gridDim.x - 1 - blockIdx.x) * 2 * kTile;   // heaviest (causal) CTAs first
+    const SeqInfo si = seq_info(p, b);
+    if (!si.ok || m0 >= si.len_q) return;
+    const int hk = h / p.G;
+
+    // Key tiles per query tile (causal: up to the diagonal); 0 for an empty tile.
+    int n_t[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int r0 = m0 + t * kTile;
+        int kend = si.len_k;
+        if (p.causal) kend = min(kend, r0 + kTile);
+        n_t[t] = (r0 < si.len_q) ? (kend + kTile - 1) / kTile : 0;
+    }
+    const int n_all = max(n_t[0], n_t[1]);
+
+    if (tid == 0) {
+        for (int i = 0; i < L::kNumBars; ++i) {
+            uint32_t cnt = 1;
+            if (i == L::kBarPFull || i == L::kBarPFull + 1) cnt = kTile;
+            mbar_init(bar(i), cnt);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    const int row_base = si.row0;      // sequence start in the packed row dimension
+    const int bcoord = p.varlen ? 0 : b;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&maps.q);
+            tma_prefetch_desc(&maps.k);
+            tma_prefetch_desc(&maps.v);
+            mbar_arrive_expect_tx(bar(L::kBarQ), 2 * L::kTileBytes);
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int c = 0; c < L::kBlocks; ++c)
+                    tma_load_4d(sbase + L::kQ + t * L::kTileBytes + c * 16384, &maps.q, 64 * c, h,
+                                row_base + m0 + t * kTile, bcoord, bar(L::kBarQ));
+            int issued = 0;
+            for (int j = 0; j < n_all && !*abort_flag; ++j) {
+                for (int which = 0; which < 2; ++which) {
+                    const int li = 2 * j + which;
+                    const int s = li % L::kStages, r = li / L::kStages;
+                    if (!mbar_wait(bar(L::kBarKVEmpty + s), (r & 1) ^ 1, abort_flag)) break;
+                    mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kTileBytes);
+                    const CUtensorMap* m = which ? &maps.v : &maps.k;
+#pragma unroll
+                    for (int c = 0; c < L::kBlocks; ++c)
+                        tma_load_4d(sbase + L::kKV + s * L::kTileBytes + c * 16384, m, 64 * c, hk,
+                                    row_base + j * kTile, bcoord, bar(L::kBarKVFull + s));
+                    issued = li + 1;
+                }
+            }
+            if (*abort_flag) {
+                // Let the copies in flight land before the CTA exits.
+                for (int li = max(0, issued - L::kStages); li < issued; ++li) {
+                    const int s = li % L::kStages, r = li / L::kStages;
+                    volatile int no_abort = 0;
+                    mbar_wait(bar(L::kBarKVFull + s), r & 1, &no_abort);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ UMMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
+            const uint32_t colS[2] = {L::kColS0, L::kColS1};
+            const uint32_t colO[2] = {L::kColO0, L::kColO1};
+            auto kv_stage = [&](int li) { return li % L::kStages; };
+            auto kv_par = [&](int li) { return (uint32_t)((li / L::kStages) & 1); };
+            auto issue_qk = [&](int t, int j) {
+                const int s = kv_stage(2 * j);
+                const uint32_t qa = sbase + L::kQ + t * L::kTileBytes;
+                const uint32_t ka = sbase + L::kKV + s * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tmem + colS[t], smem_desc(qa + off, 16, 1024, kSwizzle128B),
+                           smem_desc(ka + off, 16, 1024, kSwizzle128B), idesc_qk, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int t, int j) {
+                const int s = kv_stage(2 * j + 1);
+                const uint32_t va = sbase + L::kKV + s * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    mma_ts(tmem + colO[t], tmem + colS[t] + 64 + kk * 8,
+                           smem_desc(va + kk * 2048, 16384, 1024, kSwizzle128B), idesc_pv,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = mbar_wait(bar(L::kBarQ), 0, abort_flag);
+            if (ok && n_all > 0) {
+                ok = mbar_wait(bar(L::kBarKVFull + kv_stage(0)), kv_par(0), abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < 2; ++t) {
+                        if (n_t[t] > 0) {
+                            issue_qk(t, 0);
+                            mma_commit(bar(L::kBarSFull + t));
+                        }
+                    }
+                    mma_commit(bar(L::kBarKVEmpty + kv_stage(0)));
+                }
+            }
+            for (int j = 0; ok && j < n_all; ++j) {
+                const int lv = 2 * j + 1, lk = 2 * j + 2;
+                if (!(ok = mbar_wait(bar(L::kBarKVFull + kv_stage(lv)), kv_par(lv), abort_flag)))
+                    break;
+                const bool next = j + 1 < n_all;
+                if (next && !(ok = mbar_wait(bar(L::kBarKVFull + kv_stage(lk)), kv_par(lk),
+                                             abort_flag)))
+                    break;
+                for (int t = 0; t < 2; ++t) {
+                    if (j < n_t[t]) {
+                        if (!(ok = mbar_wait(bar(L::kBarPFull + t), j & 1, abort_flag))) break;
+                        tc_fence_after();
+                        issue_pv(t, j);
+                        mma_commit(bar(L::kBarPVDone + t));
+                    }
+                    if (t == 1) mma_commit(bar(L::kBarKVEmpty + kv_stage(lv)));
+                    if (j + 1 < n_t[t]) {
+                        // P_t(j) and S_t(j+1) share TMEM columns: O_t's MMA must be done.
+                        if (!(ok = mbar_wait(bar(L::kBarPVDone + t), j & 1, abort_flag))) break;
+                        tc_fence_after();
+                        issue_qk(t, j + 1);
+                        mma_commit(bar(L::kBarSFull + t));
+                    }
+                }
+                if (ok && next) mma_commit(bar(L::kBarKVEmpty + kv_stage(lk)));
+            }
+            if (!ok) {
+                mma_commit(bar(L::kBarDrain));
+                volatile int no_abort = 0;
+                mbar_wait(bar(L::kBarDrain), 0, &no_abort);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax WGs
+        const int t = warp >> 2;                    // query tile of this warpgroup
+        const int wq = warp & 3;                    // TMEM lane quarter
+        const int r_local = wq * 32 + lane;
+        const int i = m0 + t * kTile + r_local;     // query row in the sequence
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + (t ? L::kColS1 : L::kColS0);
+        const uint32_t tO = tmem + lane_off + (t ? L::kColO1 : L::kColO0);
+        const int n_mine = n_t[t];
+        const int r0_tile = m0 + t * kTile;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+
+        for (int j = 0; j < n_mine; ++j) {
+            ok = mbar_wait(bar(L::kBarSFull + t), j & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float x[kTile];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, reinterpret_cast<uint32_t*>(x) + 32 * c);
+            tmem_wait_ld();
+
+            const int n0 = j * kTile;
+            const bool pred = (n0 + kTile > si.len_k) ||
+                              (p.causal && n0 + kTile - 1 > r0_tile) ||
+                              (p.mask_kind != MASK_NONE);
+            float mt = -INFINITY;
+            if (pred) {
+#pragma unroll
+                for (int c = 0; c < kTile; ++c) {
+                    x[c] = logit_log2(p, x[c], b, h, i, n0 + c, si.len_q, si.len_k);
+                    mt = fmaxf(mt, x[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kTile; ++c) {
+                    x[c] *= p.scale_log2;
+                    mt = fmaxf(mt, x[c]);
+                }
+            }
+            // Online max: always m_new = max(m_ref, m_tile); lazy threshold 8.
+            const float m_new = fmaxf(m_ref, mt);
+            bool rescale;
+            if (m_new == -INFINITY) {
+                rescale = false;
+            } else if (p.lazy && m_ref != -INFINITY && mt - m_ref <= kLazyTau) {
+                rescale = false;
+            } else {
+                rescale = true;
+            }
+            float corr = 1.f;
+            if (rescale) {
+                corr = ex2(m_ref - m_new);          // m_ref = -inf -> 0
+                l *= corr;
+                // O holds data only after the first PV; a row whose m_ref was
+                // -inf has O = 0 there and needs no correction.
+                if (j == 0 || m_ref == -INFINITY) corr = 1.f;
+                m_ref = m_new;
+            }
+            const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ex2(fminf(x[32 * c + 2 * e] - ms, kLazyTau));
+                    const float p1 = ex2(fminf(x[32 * c + 2 * e + 1] - ms, kLazyTau));
+                    l += p0 + p1;
+                    pk[e] = pack_bf16(p0, p1);
+                }
+                tmem_st16(tS + 64 + 16 * c, pk);
+            }
+            // Rescale O_t in TMEM (its previous MMA has completed: the commit that
+            // signalled S_t(j) was issued after it).
+            if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32 * c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+                    tmem_st32(tO + 32 * c, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarPFull + t));
+        }
+
+        // Epilogue.
+        const bool store = ok && i < si.len_q;
+        bf16* orow = p.out + b * p.out_b + static_cast<int64_t>(row_base + i) * p.out_s + h * p.out_h;
+        if (ok && n_mine > 0) {
+            ok = mbar_wait(bar(L::kBarPVDone + t), (n_mine - 1) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+        }
+        if (ok) {
+            const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (n_mine > 0) {
+                    tmem_ld32(tO + 32 * c, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                if (store) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv,
+                                          __uint_as_float(o[2 * e + 1]) * inv);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            if (store)
+                p.lse[b * p.lse_b + h * p.lse_h + row_base + i] =
+                    l > 0.f ? (m_ref + lg2(l)) * kLn2 : 0.f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+    if (tid == 0 && *abort_flag) set_error(p.err, DEV_E_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 4-D map over a bf16 [B, S, H, D] view (dims innermost first: D, H, S, B),
+// box = 64 x 1 x 128 x 1, 128-byte swizzle.  Rows past S read as zero.
+bool make_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t S, int64_t B,
+              int64_t sh, int64_t ss, int64_t sb) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)(sh * 2), (cuuint64_t)(ss * 2), (cuuint64_t)(sb * 2)};
+    // Strides of size-1 dims are irrelevant; keep them legal (16-byte multiples).
+    if (H == 1) strides[0] = (cuuint64_t)(D * 2);
+    if (B == 1) strides[2] = strides[1] * (cuuint64_t)(S > 0 ? S : 1);
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_fwd_sm100_d(const Problem& p, cudaStream_t stream) {
+    using L = FwdLayout<D>;
+    if (p.B == 0 || p.Sq == 0) return cudaSuccess;
+    FwdMaps maps;
+    const int64_t S = p.varlen ? p.T : p.Sq;
+    const int64_t Sk = p.varlen ? p.T : p.Sk;
+    const int64_t Bm = p.varlen ? 1 : p.B;
+    // An empty key set still needs legal maps; point them at q.
+    const bool no_keys = Sk == 0;
+    if (!make_map(&maps.q, p.q, D, p.Hq, S, Bm, p.q_h, p.q_s, p.q_b)) return cudaErrorInvalidValue;
+    if (!make_map(&maps.k, no_keys ? p.q : p.k, D, no_keys ? p.Hq : p.Hkv, no_keys ? S : Sk, Bm,
+                  no_keys ? p.q_h : p.k_h, no_keys ? p.q_s : p.k_s, no_keys ? p.q_b : p.k_b))
+        return cudaErrorInvalidValue;
+    if (!make_map(&maps.v, no_keys ? p.q : p.v, D, no_keys ? p.Hq : p.Hkv, no_keys ? S : Sk, Bm,
+                  no_keys ? p.q_h : p.v_h, no_keys ? p.q_s : p.v_s, no_keys ? p.q_b : p.v_b))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(fwd_sm100_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.Sq + 2 * kTile - 1) / (2 * kTile), p.Hq, p.B);
+    fwd_sm100_kernel<D><<<grid, kFwdThreads, L::kBytes, stream>>>(p, maps);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_sm100(const Problem& p, cudaStream_t stream) {
+    return p.D == 64 ? launch_fwd_sm100_d<64>(p, stream) : launch_fwd_sm100_d<128>(p, stream);
+}
+
+}  // namespace attn
