@@ -102,7 +102,8 @@ enum {
     ATTN_E_CUDA = -7,         /* a CUDA runtime call failed                    */
     ATTN_E_TIMEOUT = -8,      /* device: a bounded wait gave up                */
     ATTN_E_SEQLENS = -9,      /* device: cu_seqlens malformed / over max_seqlen*/
-    ATTN_E_ARG = -10          /* null pointer or non-finite scale              */
+    ATTN_E_ARG = -10,         /* null pointer or non-finite scale              */
+    ATTN_E_INTERNAL = -11     /* device: an internal invariant failed          */
 };
 
 /* Flags (bitwise OR). */
@@ -173,13 +174,19 @@ int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t
 
 /*
  * attn_get_error - synchronises `stream`, then returns and clears the error
- * word of the current device: ATTN_OK, ATTN_E_SEQLENS or ATTN_E_TIMEOUT
+ * word of the current device: ATTN_OK, ATTN_E_SEQLENS, ATTN_E_TIMEOUT or
+ * ATTN_E_INTERNAL
  * (ATTN_E_CUDA if the synchronisation itself failed).
  */
 int attn_get_error(attn_stream_t stream);
 
 /* attn_strerror - static, human-readable text for a return code. */
 const char* attn_strerror(int code);
+
+/* attn_last_cuda_error - the CUDA runtime error behind the last ATTN_E_CUDA
+ * returned to this thread ("" if none): which step failed, the error name and
+ * its text.  The string is owned by the library (thread-local storage). */
+const char* attn_last_cuda_error(void);
 
 /* attn_version - library version as major * 10000 + minor * 100 + patch. */
 int attn_version(void);

@@ -13,12 +13,13 @@ ATTN_EAGER_RESCALE = 2
 ERRORS = {
     0: "ATTN_OK", -1: "ATTN_E_DTYPE", -2: "ATTN_E_SHAPE", -3: "ATTN_E_LAYOUT",
     -4: "ATTN_E_DEVICE", -5: "ATTN_E_UNSUPPORTED", -6: "ATTN_E_WORKSPACE",
-    -7: "ATTN_E_CUDA", -8: "ATTN_E_TIMEOUT", -9: "ATTN_E_SEQLENS", -10: "ATTN_E_ARG",
+    -7: "ATTN_E_CUDA", -8: "ATTN_E_TIMEOUT", -9: "ATTN_E_SEQLENS", -10: "ATTN_E_ARG", -11: "ATTN_E_INTERNAL",
 }
 
 # Every symbol the header declares.
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_error",
-           "attn_strerror", "attn_version", "attn_profile_events", "attn_launch_count")
+           "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_profile_events",
+           "attn_launch_count")
 
 ATTN_STAGE_FWD, ATTN_STAGE_BWD_PREPROCESS, ATTN_STAGE_BWD_MAIN, ATTN_STAGE_BWD_DQ = 0, 1, 2, 3
 
@@ -67,6 +68,8 @@ def load():
     lib.attn_get_error.argtypes = [ctypes.c_void_p]
     lib.attn_strerror.restype = ctypes.c_char_p
     lib.attn_strerror.argtypes = [ctypes.c_int]
+    lib.attn_last_cuda_error.restype = ctypes.c_char_p
+    lib.attn_last_cuda_error.argtypes = []
     lib.attn_version.restype = ctypes.c_int
     lib.attn_version.argtypes = []
     lib.attn_profile_events.restype = ctypes.c_int
@@ -80,7 +83,10 @@ def load():
 class AttnError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        text = load().attn_strerror(code).decode()
+        lib = load()
+        text = lib.attn_strerror(code).decode()
+        if code == -7:
+            text += "; " + lib.attn_last_cuda_error().decode()
         super().__init__("%s failed: %s (%s)" % (where, ERRORS.get(code, code), text))
 
 

@@ -13,6 +13,7 @@
 #include <math.h>
 #include <mutex>
 #include <stdint.h>
+#include <stdio.h>
 
 #include "../../include/attn_gb300.h"
 #include "attn_internal.h"
@@ -39,6 +40,13 @@ int* error_word(int dev) {
 }
 
 std::atomic<unsigned long long> g_launches{0};
+thread_local char g_cuda_detail[256] = "";
+
+int cuda_fail(cudaError_t e, const char* what) {
+    snprintf(g_cuda_detail, sizeof(g_cuda_detail), "%s: %s (%s)", what, cudaGetErrorName(e),
+             cudaGetErrorString(e));
+    return ATTN_E_CUDA;
+}
 cudaEvent_t g_prof[ATTN_STAGE_COUNT][2] = {};
 
 // Launch one stage: optional profiling events around it, launch accounting.
@@ -46,11 +54,12 @@ template <class F>
 int run_stage(int stage, cudaStream_t st, F&& launch) {
     cudaEvent_t a = stage >= 0 ? g_prof[stage][0] : nullptr;
     cudaEvent_t b = stage >= 0 ? g_prof[stage][1] : nullptr;
-    if (a && cudaEventRecord(a, st) != cudaSuccess) return ATTN_E_CUDA;
-    const cudaError_t e = launch();
-    if (e != cudaSuccess) return ATTN_E_CUDA;
+    cudaError_t e;
+    if (a && (e = cudaEventRecord(a, st)) != cudaSuccess) return cuda_fail(e, "event record");
+    e = launch();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    if (b && cudaEventRecord(b, st) != cudaSuccess) return ATTN_E_CUDA;
+    if (b && (e = cudaEventRecord(b, st)) != cudaSuccess) return cuda_fail(e, "event record");
     return ATTN_OK;
 }
 
@@ -76,6 +85,8 @@ int check_input(const attn_tensor_t* t, int rank) {
 }
 
 bool is_contiguous(const attn_tensor_t* t) {
+    for (int i = 0; i < t->ndim; ++i)
+        if (t->shape[i] == 0) return true;   // no elements: any strides describe it
     int64_t s = 1;
     for (int i = t->ndim - 1; i >= 0; --i) {
         if (t->shape[i] != 1 && t->stride[i] != s) return false;
@@ -399,7 +410,10 @@ extern "C" int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const at
     p.delta = reinterpret_cast<float*>(ws + w.delta);
     p.lse2 = reinterpret_cast<float*>(ws + w.lse2);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (!det && w.delta > 0) ATTN_TRY(cuda_rc(cudaMemsetAsync(ws + w.acc, 0, w.delta, st)));
+    if (!det && w.delta > 0) {
+        const cudaError_t e = cudaMemsetAsync(ws + w.acc, 0, w.delta, st);
+        if (e != cudaSuccess) return cuda_fail(e, "workspace zero-fill");
+    }
     ATTN_TRY(run_stage(ATTN_STAGE_BWD_PREPROCESS, st, [&] { return launch_bwd_preprocess(p, st); }));
     if (s.varlen) ATTN_TRY(run_stage(-1, st, [&] { return launch_zero_trailing_bwd(p, st); }));
     ATTN_TRY(run_stage(ATTN_STAGE_BWD_MAIN, st, [&] { return launch_bwd_main(p, !det, st); }));
@@ -436,6 +450,7 @@ extern "C" const char* attn_strerror(int code) {
         case ATTN_E_TIMEOUT: return "a bounded device wait gave up";
         case ATTN_E_SEQLENS: return "cu_seqlens malformed or a sequence exceeds max_seqlen";
         case ATTN_E_ARG: return "null pointer or non-finite scale";
+        case ATTN_E_INTERNAL: return "an internal invariant failed on the device";
         default: return "unknown error code";
     }
 }
@@ -448,6 +463,8 @@ extern "C" int attn_profile_events(int stage, void* before, void* after) {
     g_prof[stage][1] = static_cast<cudaEvent_t>(after);
     return ATTN_OK;
 }
+
+extern "C" const char* attn_last_cuda_error(void) { return g_cuda_detail; }
 
 extern "C" unsigned long long attn_launch_count(void) {
     return g_launches.load(std::memory_order_relaxed);

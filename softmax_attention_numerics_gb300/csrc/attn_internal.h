@@ -2,6 +2,7 @@
 // kernels.  Not part of the public ABI (include/attn_gb300.h is).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -62,11 +63,20 @@ struct Problem {
 // Error codes written to the device error word (match include/attn_gb300.h).
 constexpr int DEV_E_TIMEOUT = -8;
 constexpr int DEV_E_SEQLENS = -9;
+constexpr int DEV_E_INTERNAL = -11;
+
+// TMA tensor map over a bf16 [B, S, H, D] view (dims innermost first: D, H,
+// S, B; strides in elements), box 64 x 1 x 128 x 1, 128-byte swizzle.
+// Rows past S read as zero and are clipped on store.
+bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t S, int64_t B,
+                   int64_t sh, int64_t ss, int64_t sb);
 
 // Launchers (each enqueues on `stream`, returns cudaGetLastError()).
 cudaError_t launch_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(const Problem& p, bool with_dq_atomics, cudaStream_t stream);
+cudaError_t launch_fwd_sm100(const Problem& p, cudaStream_t stream);
+cudaError_t launch_bwd_main_sm100(const Problem& p, bool with_dq_atomics, cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_deterministic(const Problem& p, cudaStream_t stream);
 cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream);

@@ -2,7 +2,7 @@
 //   bwd_preprocess  Delta = rowsum(dO o O) in fp32 and lse2 = lse * log2(e)
 //   dq_convert      dq = bf16(dq_acc * scale)
 //   zero_trailing   rows >= cu[nseq] of a packed varlen buffer: out = 0 and
-//                   lse = 0 (forward), dk = dv = 0 (backward).  Rows that no
+//                   lse = 0 (forward), dq = dk = dv = 0 (backward).  Rows that no
 //                   tile visits must still be written (PFCCLab/cudnn-frontend
 //                   PR #9, section 2; flash-dmattn PR #122, Root Cause 1).
 // All are grid-stride loops sized to a multiple of the SM count.
@@ -111,6 +111,7 @@ __global__ void zero_trailing_fwd_kernel(const Problem p) {
 
 __global__ void zero_trailing_bwd_kernel(const Problem p) {
     const int64_t r0 = trailing_start(p);
+    zero_rows_bf16(p.dq, r0, p.T, p.Hq, p.D);
     zero_rows_bf16(p.dk, r0, p.T, p.Hkv, p.D);
     zero_rows_bf16(p.dv, r0, p.T, p.Hkv, p.D);
 }
@@ -156,7 +157,7 @@ cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream) {
 
 cudaError_t launch_zero_trailing_bwd(const Problem& p, cudaStream_t stream) {
     if (!p.varlen || p.T == 0) return cudaSuccess;
-    zero_trailing_bwd_kernel<<<grid_for(static_cast<int64_t>(p.T) * p.Hkv * p.D / 8, 256), 256,
+    zero_trailing_bwd_kernel<<<grid_for(static_cast<int64_t>(p.T) * p.Hq * p.D / 8, 256), 256,
                                0, stream>>>(p);
     return cudaGetLastError();
 }

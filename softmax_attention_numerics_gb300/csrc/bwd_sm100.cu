@@ -1,0 +1,493 @@
+// Attention backward (main kernel) for sm_103a: TMA + tcgen05 + TMEM.
+//
+// One CTA = 128 keys (one K/V tile) of one (batch/sequence, kv head).  It
+// walks every q head of the GQA group and every 128-row query tile that can
+// see its keys (causal: tiles at or below the diagonal):
+//     S^T  = K Q_i^T            (TMEM, 128 x 128 fp32)
+//     dP^T = V dO_i^T           (TMEM)
+//     P^T  = exp2(min(S^T*scale*log2e + mask - lse2, 0)), with the forward's
+//            predicates: partial last key tile, query rows past the
+//            sequence, causal pairs, the mask (OpenWAM PR #64: an unmasked
+//            partial key tile turns exp(0 - lse) into inf once lse < -88.7).
+//            The clamp at 0 holds because P <= 1 (PFCCLab/cudnn-frontend PR #9,
+//            section 3).  Hidden entries are 0 by selection.
+//     dS^T = P^T o (dP^T - Delta)
+//     dV  += P^T dO_i, dK += dS^T Q_i       (TMEM accumulators, no atomics)
+//     dQ_i = dS K  -> fp32 vector reductions into the dQ workspace
+// Warps: 0-3 compute P^T / dS^T (thread = key row = TMEM lane); 4-7 read dQ_i
+// out of TMEM (thread = query row) and reduce it into global memory while the
+// next tile's MMAs run; 8 = TMA producer (+ lse2 / Delta vectors); 9 = TMEM
+// allocator and UMMA issuer.
+// TMEM: dV | dK (D columns each) | S^T | dP^T (128 each).  P^T (bf16) is
+// written over the first half of S^T and dS^T over the first half of dP^T;
+// dQ_i lands in the second halves (columns 64-127 of S^T, then of dP^T).
+//
+// Epilogue (PFCCLab/cudnn-frontend PR #9, section 1): every thread writes its
+// dK / dV row into a shared staging tile, fences its own writes for the async
+// proxy, the warpgroup meets at a named barrier, ONE thread issues the bulk
+// tensor store and only that thread waits on its bulk group, and the group
+// meets again before the tile could be reused.  A partial key tile of a
+// packed varlen sequence is stored with predicated plain stores instead, so
+// the neighbouring sequence's rows are never touched.
+#include "sm100_ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBwdThreads = 320;
+constexpr int kT = 128;
+
+template <int D>
+struct BwdLayout {
+    static constexpr int kBlocks = D / 64;
+    static constexpr int kTileBytes = kT * D * 2;
+    static constexpr int kK = 0;
+    static constexpr int kV = kTileBytes;
+    static constexpr int kQ = 2 * kTileBytes;           // 2 stages
+    static constexpr int kDO = 4 * kTileBytes;          // 2 stages
+    static constexpr int kDS = 6 * kTileBytes;          // dS as [128 keys][128 q] bf16
+    static constexpr int kVec = kDS + kT * kT * 2;      // lse2[2][128], delta[2][128]
+    static constexpr int kBar = kVec + 4 * kT * 4;
+    static constexpr int kBarKV = 0;
+    static constexpr int kBarQFull = 1;                 // [2]
+    static constexpr int kBarQEmpty = 3;                // [2]
+    static constexpr int kBarS = 5;
+    static constexpr int kBarDP = 6;
+    static constexpr int kBarP = 7;
+    static constexpr int kBarDQFull = 8;
+    static constexpr int kBarDQRead = 9;
+    static constexpr int kBarAcc = 10;
+    static constexpr int kBarDrain = 11;
+    static constexpr int kNumBars = 12;
+    static constexpr int kMisc = kBar + kNumBars * 8;
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
+};
+
+struct BwdMaps {
+    CUtensorMap k, v, q, dout, dk, dv;
+};
+
+// Write one 32-column chunk of a row into a TMA-layout staging tile
+// ([blocks][128 rows][128 B], 16-byte chunks XOR-swizzled by row mod 8).
+__device__ __forceinline__ void stage_row_chunk(uint8_t* tile, int row, int col0,
+                                                const uint32_t* pk16) {
+    const int blk = col0 >> 6;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int ch = ((col0 & 63) >> 3) + v;
+        uint4* dst = reinterpret_cast<uint4*>(tile + blk * 16384 + row * 128 + ((ch ^ (row & 7)) << 4));
+        *dst = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+    }
+}
+
+template <int D>
+__global__ void __maxnreg__(200) bwd_sm100_kernel(const Problem p, const __grid_constant__ BwdMaps maps,
+                                                  int with_dq) {
+    using L = BwdLayout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + L::kBar + 8u * i; };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+    float* vec = reinterpret_cast<float*>(smem + L::kVec);   // lse2[s][128] at s*256, delta at +128
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int n0 = blockIdx.x * kT;
+    const SeqInfo si = seq_info(p, b);
+    if (!si.ok || n0 >= si.len_k) return;
+    if ((sbase & 1023u) != 0) {            // swizzle atoms need 1 KiB alignment
+        if (tid == 0) set_error(p.err, DEV_E_INTERNAL);
+        return;
+    }
+
+    const int mt_first = p.causal ? n0 / kT : 0;
+    const int mt_count = (si.len_q + kT - 1) / kT;
+    const int per_head = max(mt_count - mt_first, 0);
+    const int n_iter = per_head * p.G;
+    const int row_base = si.row0;
+    const int bcoord = p.varlen ? 0 : b;
+
+    if (tid == 0) {
+        for (int i = 0; i < L::kNumBars; ++i) {
+            uint32_t cnt = 1;
+            if (i == L::kBarQFull || i == L::kBarQFull + 1) cnt = 33;
+            if (i == L::kBarP || i == L::kBarDQRead) cnt = kT;
+            mbar_init(bar(i), cnt);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    auto iter_tile = [&](int it, int* h, int* m0) {
+        const int gi = it / per_head;
+        *m0 = (mt_first + it % per_head) * kT;
+        *h = hk * p.G + gi;
+    };
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer (whole warp)
+        bool ok = true;
+        if (lane == 0) {
+            tma_prefetch_desc(&maps.k);
+            tma_prefetch_desc(&maps.q);
+            mbar_arrive_expect_tx(bar(L::kBarKV), 2 * L::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < L::kBlocks; ++c) {
+                tma_load_4d(sbase + L::kK + c * 16384, &maps.k, 64 * c, hk, row_base + n0, bcoord,
+                            bar(L::kBarKV));
+                tma_load_4d(sbase + L::kV + c * 16384, &maps.v, 64 * c, hk, row_base + n0, bcoord,
+                            bar(L::kBarKV));
+            }
+        }
+        int issued = 0;
+        for (int it = 0; it < n_iter; ++it) {
+            const int s = it & 1, r = it >> 1;
+            ok = mbar_wait(bar(L::kBarQEmpty + s), (r & 1) ^ 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            int h, m0;
+            iter_tile(it, &h, &m0);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(L::kBarQFull + s), 2 * L::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < L::kBlocks; ++c) {
+                    tma_load_4d(sbase + L::kQ + s * L::kTileBytes + c * 16384, &maps.q, 64 * c, h,
+                                row_base + m0, bcoord, bar(L::kBarQFull + s));
+                    tma_load_4d(sbase + L::kDO + s * L::kTileBytes + c * 16384, &maps.dout, 64 * c,
+                                h, row_base + m0, bcoord, bar(L::kBarQFull + s));
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int q = 4 * lane + e;
+                const int i = m0 + q;
+                const int64_t li = b * p.lse_b + h * p.lse_h + row_base + i;
+                const bool in = i < si.len_q;
+                vec[s * 256 + q] = in ? p.lse2[li] : 0.f;
+                vec[s * 256 + 128 + q] = in ? p.delta[li] : 0.f;
+            }
+            mbar_arrive(bar(L::kBarQFull + s));
+            issued = it + 1;
+        }
+        if (*abort_flag && lane == 0) {
+            volatile int no_abort = 0;
+            mbar_wait(bar(L::kBarKV), 0, &no_abort);
+            for (int it = max(0, issued - 2); it < issued; ++it)
+                mbar_wait(bar(L::kBarQFull + (it & 1)), (it >> 1) & 1, &no_abort);
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ UMMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_kmaj = idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
+            constexpr uint32_t id_acc = idesc_bf16(128, D, 0, 1);      // dV, dK (B MN-major)
+            constexpr uint32_t id_dq = idesc_bf16(128, 64, 1, 1);      // dQ halves
+            const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP;
+            const uint32_t tDV = tmem + L::kColDV, tDK = tmem + L::kColDK;
+            bool ok = mbar_wait(bar(L::kBarKV), 0, abort_flag);
+            for (int it = 0; ok && it < n_iter; ++it) {
+                const int s = it & 1, r = it >> 1;
+                if (!(ok = mbar_wait(bar(L::kBarQFull + s), r & 1, abort_flag))) break;
+                // S^T / dP^T columns are free once the previous dQ has been read out
+                // (its commit covered every earlier MMA, including dV and dK).
+                if (it > 0 && !(ok = mbar_wait(bar(L::kBarDQRead), (it - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                const uint32_t qa = sbase + L::kQ + s * L::kTileBytes;
+                const uint32_t da = sbase + L::kDO + s * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tS, smem_desc(sbase + L::kK + off, 16, 1024, kSwizzle128B),
+                           smem_desc(qa + off, 16, 1024, kSwizzle128B), id_kmaj, kk > 0);
+                }
+                mma_commit(bar(L::kBarS));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tDP, smem_desc(sbase + L::kV + off, 16, 1024, kSwizzle128B),
+                           smem_desc(da + off, 16, 1024, kSwizzle128B), id_kmaj, kk > 0);
+                }
+                mma_commit(bar(L::kBarDP));
+                if (!(ok = mbar_wait(bar(L::kBarP), it & 1, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk) {
+                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts(tDV, tS + kk * 8, smem_desc(da + kk * 2048, 16384, 1024, kSwizzle128B),
+                           id_acc, acc);
+                    mma_ts(tDK, tDP + kk * 8, smem_desc(qa + kk * 2048, 16384, 1024, kSwizzle128B),
+                           id_acc, acc);
+                }
+                mma_commit(bar(L::kBarQEmpty + s));
+                if (with_dq) {
+#pragma unroll
+                    for (int hh = 0; hh < L::kBlocks; ++hh) {
+                        const uint32_t dst = (hh == 0 ? tS : tDP) + 64;
+#pragma unroll
+                        for (int kk = 0; kk < kT / 16; ++kk)
+                            mma_ss(dst, smem_desc(sbase + L::kDS + kk * 2048, 16384, 1024, kSwizzle128B),
+                                   smem_desc(sbase + L::kK + hh * 16384 + kk * 2048, 16384, 1024,
+                                             kSwizzle128B),
+                                   id_dq, kk > 0);
+                    }
+                }
+                mma_commit(bar(L::kBarDQFull));
+            }
+            mma_commit(bar(L::kBarAcc));
+            if (!ok) {
+                mma_commit(bar(L::kBarDrain));
+                volatile int no_abort = 0;
+                mbar_wait(bar(L::kBarDrain), 0, &no_abort);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ P^T / dS^T
+        const int r = warp * 32 + lane;             // key row in the tile = TMEM lane
+        const int j = n0 + r;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_off + L::kColS;
+        const uint32_t tDP = tmem + lane_off + L::kColDP;
+        uint8_t* ds_tile = smem + L::kDS;
+        bool ok = true;
+        for (int it = 0; it < n_iter; ++it) {
+            const int s = it & 1;
+            int h, m0;
+            iter_tile(it, &h, &m0);
+            // q_full[s] also publishes the producer's lse2 / Delta vectors.
+            ok = mbar_wait(bar(L::kBarQFull + s), (it >> 1) & 1, abort_flag) &&
+                 mbar_wait(bar(L::kBarS), it & 1, abort_flag) &&
+                 mbar_wait(bar(L::kBarDP), it & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float* lse2 = vec + s * 256;
+            const float* del = lse2 + 128;
+            const bool pred = (n0 + kT > si.len_k) || (m0 + kT > si.len_q) ||
+                              (p.causal && n0 + kT - 1 > m0) || (p.mask_kind != MASK_NONE);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], dv[32];
+                tmem_ld32(tS + 32 * c, sv);
+                tmem_ld32(tDP + 32 * c, dv);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float pr[2], ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int q = 32 * c + e + u;
+                        const float acc = __uint_as_float(sv[e + u]);
+                        const float x = pred ? logit_log2(p, acc, b, h, m0 + q, j, si.len_q, si.len_k)
+                                             : acc * p.scale_log2;
+                        const bool vis = x != -INFINITY;
+                        const float pv = ex2(fminf(x - lse2[q], 0.f));
+                        pr[u] = vis ? pv : 0.f;
+                        ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - del[q]) : 0.f;
+                    }
+                    pk[e >> 1] = pack_bf16(pr[0], pr[1]);
+                    dk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                }
+                tmem_st16(tS + 16 * c, pk);
+                tmem_st16(tDP + 16 * c, dk);
+                if (with_dq) stage_row_chunk(ds_tile, r, 32 * c, dk);
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();      // dS in shared memory -> the dQ MMA
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarP));
+        }
+        // dV epilogue: staging tile = the dS buffer (free once every MMA is done).
+        if (ok) {
+            ok = mbar_wait(bar(L::kBarAcc), 0, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            const bool tma_path = !p.varlen || n0 + kT <= si.len_k;
+            bf16* grow = p.dv + b * p.dk_b + static_cast<int64_t>(row_base + j) * p.dk_s + hk * p.dk_h;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (n_iter > 0) {
+                    tmem_ld32(tmem + lane_off + L::kColDV + 32 * c, o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+                if (tma_path) {
+                    stage_row_chunk(ds_tile, r, 32 * c, pk);
+                } else if (j < si.len_k) {
+                    uint4* dst = reinterpret_cast<uint4*>(grow + 32 * c);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            if (tma_path) {
+                fence_proxy_async_smem();   // each writer: its stores -> async proxy
+                named_bar_sync(1, 128);     // all 128 rows are in the staging tile
+                if (r == 0) {
+#pragma unroll
+                    for (int c = 0; c < L::kBlocks; ++c)
+                        tma_store_4d(&maps.dv, sbase + L::kDS + c * 16384, 64 * c, hk, row_base + n0,
+                                     bcoord);
+                    bulk_commit();
+                    bulk_wait_read_all();   // only the committing thread may wait
+                }
+                named_bar_sync(1, 128);     // staging tile no longer read
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ dQ read-out (warps 4-7)
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;               // query row in the tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        bool ok = true;
+        for (int it = 0; it < n_iter; ++it) {
+            int h, m0;
+            iter_tile(it, &h, &m0);
+            ok = mbar_wait(bar(L::kBarDQFull), it & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float dq[D];
+            if (with_dq) {
+#pragma unroll
+                for (int hh = 0; hh < L::kBlocks; ++hh) {
+                    const uint32_t src = tmem + lane_off + (hh == 0 ? L::kColS : L::kColDP) + 64;
+                    tmem_ld32(src, reinterpret_cast<uint32_t*>(dq) + 64 * hh);
+                    tmem_ld32(src + 32, reinterpret_cast<uint32_t*>(dq) + 64 * hh + 32);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDQRead));
+            const int i = m0 + r;
+            if (with_dq && i < si.len_q) {
+                float* dst = p.dq_acc + (b * p.acc_b + row_base + i) * static_cast<int64_t>(p.Hq) * D +
+                             static_cast<int64_t>(h) * D;
+#pragma unroll
+                for (int v = 0; v < D / 4; ++v)
+                    red_add_v4(dst + 4 * v, dq[4 * v], dq[4 * v + 1], dq[4 * v + 2], dq[4 * v + 3]);
+            }
+        }
+        // dK epilogue: staging tile = query stage 0 (free once every MMA is done).
+        if (ok) {
+            ok = mbar_wait(bar(L::kBarAcc), 0, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            const int j = n0 + r;
+            uint8_t* tile = smem + L::kQ;
+            const bool tma_path = !p.varlen || n0 + kT <= si.len_k;
+            bf16* grow = p.dk + b * p.dk_b + static_cast<int64_t>(row_base + j) * p.dk_s + hk * p.dk_h;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (n_iter > 0) {
+                    tmem_ld32(tmem + lane_off + L::kColDK + 32 * c, o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * p.scale,
+                                      __uint_as_float(o[2 * e + 1]) * p.scale);
+                if (tma_path) {
+                    stage_row_chunk(tile, r, 32 * c, pk);
+                } else if (j < si.len_k) {
+                    uint4* dst = reinterpret_cast<uint4*>(grow + 32 * c);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            if (tma_path) {
+                fence_proxy_async_smem();
+                named_bar_sync(2, 128);
+                if (r == 0) {
+#pragma unroll
+                    for (int c = 0; c < L::kBlocks; ++c)
+                        tma_store_4d(&maps.dk, sbase + L::kQ + c * 16384, 64 * c, hk, row_base + n0,
+                                     bcoord);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+                named_bar_sync(2, 128);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+    if (tid == 0 && *abort_flag) set_error(p.err, DEV_E_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int D>
+cudaError_t launch_bwd_sm100_d(const Problem& p, bool with_dq, cudaStream_t stream) {
+    using L = BwdLayout<D>;
+    if (p.B == 0 || p.Sk == 0) return cudaSuccess;
+    const int64_t Sq = p.varlen ? p.T : p.Sq;
+    const int64_t Sk = p.varlen ? p.T : p.Sk;
+    const int64_t Bm = p.varlen ? 1 : p.B;
+    // With no queries the maps are never read; keep them legal by pointing at k.
+    const bool no_q = Sq == 0;
+    BwdMaps maps;
+    bool ok = make_tile_map(&maps.k, p.k, D, p.Hkv, Sk, Bm, p.k_h, p.k_s, p.k_b) &&
+              make_tile_map(&maps.v, p.v, D, p.Hkv, Sk, Bm, p.v_h, p.v_s, p.v_b) &&
+              make_tile_map(&maps.q, no_q ? p.k : p.q, D, no_q ? p.Hkv : p.Hq, no_q ? Sk : Sq, Bm,
+                       no_q ? p.k_h : p.q_h, no_q ? p.k_s : p.q_s, no_q ? p.k_b : p.q_b) &&
+              make_tile_map(&maps.dout, no_q ? p.k : p.dout, D, no_q ? p.Hkv : p.Hq, no_q ? Sk : Sq, Bm,
+                       no_q ? p.k_h : p.do_h, no_q ? p.k_s : p.do_s, no_q ? p.k_b : p.do_b) &&
+              make_tile_map(&maps.dk, p.dk, D, p.Hkv, Sk, Bm, p.dk_h, p.dk_s, p.dk_b) &&
+              make_tile_map(&maps.dv, p.dv, D, p.Hkv, Sk, Bm, p.dk_h, p.dk_s, p.dk_b);
+    if (!ok) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(bwd_sm100_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.Sk + kT - 1) / kT, p.Hkv, p.B);
+    bwd_sm100_kernel<D><<<grid, kBwdThreads, L::kBytes, stream>>>(p, maps, with_dq ? 1 : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main_sm100(const Problem& p, bool with_dq_atomics, cudaStream_t stream) {
+    return p.D == 64 ? launch_bwd_sm100_d<64>(p, with_dq_atomics, stream)
+                     : launch_bwd_sm100_d<128>(p, with_dq_atomics, stream);
+}
+
+}  // namespace attn

@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(kThreads) fwd_mma_kernel(const Problem p) {
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_ref[2] = {-INFINITY, -INFINITY};
-    float l[2] = {0.f, 0.f};
+    float l[2] = {0.f, 0.f};     // sum of the exact probabilities (-> lse)
+    float lr[2] = {0.f, 0.f};    // sum of the bf16-rounded ones fed to P V (-> out)
     uint32_t qf[D / 16][4];
     const int row_i[2] = {m0 + warp * 16 + g, m0 + warp * 16 + g + 8};
 
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(kThreads) fwd_mma_kernel(const Problem p) {
             if (rescale) {
                 const float corr = ex2(m_ref[r] - m_new);   // m_ref = -inf -> 0
                 l[r] *= corr;
+                lr[r] *= corr;
 #pragma unroll
                 for (int n = 0; n < D / 8; ++n) {
                     o[n][2 * r] *= corr;
@@ -143,7 +145,8 @@ __global__ void __launch_bounds__(kThreads) fwd_mma_kernel(const Problem p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 pv[e] = ex2(fminf(s[n][e] - msafe[e >> 1], kLazyTau));
-                l[e >> 1] += pv[e];      // unrounded: l also feeds the lse
+                l[e >> 1] += pv[e];
+                lr[e >> 1] += bf16_round(pv[e]);
             }
             pf[n >> 1][(n & 1) * 2 + 0] = pack_bf16(pv[0], pv[1]);
             pf[n >> 1][(n & 1) * 2 + 1] = pack_bf16(pv[2], pv[3]);
@@ -166,18 +169,23 @@ __global__ void __launch_bounds__(kThreads) fwd_mma_kernel(const Problem p) {
     }
     cp_async_wait<0>();
 
-    // Epilogue: out = O / l, lse = (m_ref + log2 l) ln 2; a row with l = 0
+    // Epilogue: out = O / lr, lse = (m_ref + log2 l) ln 2; a row with l = 0
     // (no visible key) gets out = 0 and lse = 0.
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
         l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 1);
+        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 2);
     }
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         const int i = row_i[r];
         if (i >= si.len_q) continue;
-        const float inv = l[r] > 0.f ? 1.0f / l[r] : 0.f;
+        // Normalising by the sum of the rounded weights keeps out an exact
+        // weighted mean of V even when the lazy reference max lags the true
+        // one (then the largest weight is up to 2^8 and not exact in bf16).
+        const float inv = lr[r] > 0.f ? 1.0f / lr[r] : 0.f;
         bf16* og = p.out + b * p.out_b + static_cast<int64_t>(si.row0 + i) * p.out_s + h * p.out_h;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {

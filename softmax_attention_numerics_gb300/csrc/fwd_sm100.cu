@@ -22,7 +22,8 @@
 // exp2(m_ref - m_new) in TMEM; rows of the same warp that did not ask for a
 // rescale use a factor of exactly 1.  p = exp2(min(x - m_ref, 8)): the clamp
 // never fires on correct statistics (PFCCLab/cudnn-frontend PR #9, section 3).
-// Epilogue: out = O/l, lse = (m_ref + log2 l) ln 2; l = 0 gives out = 0,
+// Epilogue: out = O/lr (lr = sum of the bf16-rounded p that entered the MMA),
+// lse = (m_ref + log2 l) ln 2 (l = sum of the exact p); l = 0 gives out = 0,
 // lse = 0.  Rows past the sequence are never stored (varlen neighbours).
 #include "sm100_ptx.cuh"
 
@@ -240,7 +241,9 @@ __global__ void __maxnreg__(200)
         const uint32_t tO = tmem + lane_off + (t ? L::kColO1 : L::kColO0);
         const int n_mine = n_t[t];
         const int r0_tile = m0 + t * kTile;
-        float m_ref = -INFINITY, l = 0.f;
+        float m_ref = -INFINITY;
+        float l = 0.f;      // sum of the exact probabilities (-> lse)
+        float lr = 0.f;     // sum of the bf16-rounded probabilities fed to P V (-> out)
         bool ok = true;
 
         for (int j = 0; j < n_mine; ++j) {
@@ -287,6 +290,7 @@ __global__ void __maxnreg__(200)
             if (rescale) {
                 corr = ex2(m_ref - m_new);          // m_ref = -inf -> 0
                 l *= corr;
+                lr *= corr;
                 // O holds data only after the first PV; a row whose m_ref was
                 // -inf has O = 0 there and needs no correction.
                 if (j == 0 || m_ref == -INFINITY) corr = 1.f;
@@ -302,6 +306,7 @@ __global__ void __maxnreg__(200)
                     const float p1 = ex2(fminf(x[32 * c + 2 * e + 1] - ms, kLazyTau));
                     l += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
+                    lr += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
                 }
                 tmem_st16(tS + 64 + 16 * c, pk);
             }
@@ -333,7 +338,9 @@ __global__ void __maxnreg__(200)
             tc_fence_after();
         }
         if (ok) {
-            const float inv = l > 0.f ? 1.0f / l : 0.f;
+            // Normalise by the rounded sum: out stays an exact weighted mean of V
+            // even when the lazy reference max lags (largest weight up to 2^8).
+            const float inv = lr > 0.f ? 1.0f / lr : 0.f;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -373,44 +380,6 @@ __global__ void __maxnreg__(200)
 
 // ------------------------------------------------------------------ host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// 4-D map over a bf16 [B, S, H, D] view (dims innermost first: D, H, S, B),
-// box = 64 x 1 x 128 x 1, 128-byte swizzle.  Rows past S read as zero.
-bool make_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t S, int64_t B,
-              int64_t sh, int64_t ss, int64_t sb) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)(sh * 2), (cuuint64_t)(ss * 2), (cuuint64_t)(sb * 2)};
-    // Strides of size-1 dims are irrelevant; keep them legal (16-byte multiples).
-    if (H == 1) strides[0] = (cuuint64_t)(D * 2);
-    if (B == 1) strides[2] = strides[1] * (cuuint64_t)(S > 0 ? S : 1);
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_fwd_sm100_d(const Problem& p, cudaStream_t stream) {
     using L = FwdLayout<D>;
@@ -421,11 +390,11 @@ cudaError_t launch_fwd_sm100_d(const Problem& p, cudaStream_t stream) {
     const int64_t Bm = p.varlen ? 1 : p.B;
     // An empty key set still needs legal maps; point them at q.
     const bool no_keys = Sk == 0;
-    if (!make_map(&maps.q, p.q, D, p.Hq, S, Bm, p.q_h, p.q_s, p.q_b)) return cudaErrorInvalidValue;
-    if (!make_map(&maps.k, no_keys ? p.q : p.k, D, no_keys ? p.Hq : p.Hkv, no_keys ? S : Sk, Bm,
+    if (!make_tile_map(&maps.q, p.q, D, p.Hq, S, Bm, p.q_h, p.q_s, p.q_b)) return cudaErrorInvalidValue;
+    if (!make_tile_map(&maps.k, no_keys ? p.q : p.k, D, no_keys ? p.Hq : p.Hkv, no_keys ? S : Sk, Bm,
                   no_keys ? p.q_h : p.k_h, no_keys ? p.q_s : p.k_s, no_keys ? p.q_b : p.k_b))
         return cudaErrorInvalidValue;
-    if (!make_map(&maps.v, no_keys ? p.q : p.v, D, no_keys ? p.Hq : p.Hkv, no_keys ? S : Sk, Bm,
+    if (!make_tile_map(&maps.v, no_keys ? p.q : p.v, D, no_keys ? p.Hq : p.Hkv, no_keys ? S : Sk, Bm,
                   no_keys ? p.q_h : p.v_h, no_keys ? p.q_s : p.v_s, no_keys ? p.q_b : p.v_b))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(fwd_sm100_kernel<D>,
