@@ -85,7 +85,7 @@ __device__ __forceinline__ void stage_row_chunk(uint8_t* tile, int row, int col0
 }
 
 template <int D>
-__global__ void __maxnreg__(200) bwd_sm100_kernel(const Problem p, const __grid_constant__ BwdMaps maps,
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem p, const __grid_constant__ BwdMaps maps,
                                                   int with_dq) {
     using L = BwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem[];

@@ -63,7 +63,7 @@ struct FwdMaps {
 };
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_sm100_kernel(const Problem p, const __grid_constant__ FwdMaps maps) {
     using L = FwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
