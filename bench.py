@@ -30,7 +30,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd+bwd TFLOP/s (% of GB300 bf16 tensor peak; non-finite count = 0)"
-KERNEL_SOURCES = ("softmax_attention_numerics_gb300/csrc/bwd_mma.cu",
+KERNEL_SOURCES = ("softmax_attention_numerics_gb300/csrc/bwd_sm100.cu",
+                  "softmax_attention_numerics_gb300/csrc/sm100_ptx.cuh",
                   "softmax_attention_numerics_gb300/csrc/device_common.cuh")
 
 

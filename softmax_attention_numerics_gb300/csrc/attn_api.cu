@@ -317,7 +317,6 @@ WsLayout ws_layout(const Shapes& s, uint32_t flags) {
     return w;
 }
 
-int cuda_rc(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_E_CUDA; }
 
 }  // namespace
 }  // namespace attn

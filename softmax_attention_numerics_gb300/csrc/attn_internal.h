@@ -75,8 +75,6 @@ bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64
 cudaError_t launch_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(const Problem& p, bool with_dq_atomics, cudaStream_t stream);
-cudaError_t launch_fwd_sm100(const Problem& p, cudaStream_t stream);
-cudaError_t launch_bwd_main_sm100(const Problem& p, bool with_dq_atomics, cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_deterministic(const Problem& p, cudaStream_t stream);
 cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream);

@@ -485,7 +485,7 @@ cudaError_t launch_bwd_sm100_d(const Problem& p, bool with_dq, cudaStream_t stre
 
 }  // namespace
 
-cudaError_t launch_bwd_main_sm100(const Problem& p, bool with_dq_atomics, cudaStream_t stream) {
+cudaError_t launch_bwd_main(const Problem& p, bool with_dq_atomics, cudaStream_t stream) {
     return p.D == 64 ? launch_bwd_sm100_d<64>(p, with_dq_atomics, stream)
                      : launch_bwd_sm100_d<128>(p, with_dq_atomics, stream);
 }

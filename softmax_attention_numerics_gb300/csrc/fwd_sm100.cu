@@ -407,7 +407,7 @@ cudaError_t launch_fwd_sm100_d(const Problem& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_fwd_sm100(const Problem& p, cudaStream_t stream) {
+cudaError_t launch_fwd(const Problem& p, cudaStream_t stream) {
     return p.D == 64 ? launch_fwd_sm100_d<64>(p, stream) : launch_fwd_sm100_d<128>(p, stream);
 }
 
