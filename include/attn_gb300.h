@@ -103,7 +103,9 @@ enum {
     ATTN_E_TIMEOUT = -8,      /* device: a bounded wait gave up                */
     ATTN_E_SEQLENS = -9,      /* device: cu_seqlens malformed / over max_seqlen*/
     ATTN_E_ARG = -10,         /* null pointer or non-finite scale              */
-    ATTN_E_INTERNAL = -11     /* device: an internal invariant failed          */
+    ATTN_E_INTERNAL = -11,    /* device: an internal invariant failed          */
+    ATTN_E_TOO_LARGE = -12    /* attn_bwd_noalloc: needs more scratch than the
+                                 library's built-in array holds               */
 };
 
 /* Flags (bitwise OR). */
@@ -171,6 +173,30 @@ int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t
              const attn_tensor_t* mask, const attn_tensor_t* cu_seqlens, int32_t max_seqlen,
              int causal, float scale, attn_tensor_t* dq, attn_tensor_t* dk, attn_tensor_t* dv,
              void* workspace, size_t workspace_bytes, uint32_t flags, attn_stream_t stream);
+
+/*
+ * attn_bwd_noalloc - attn_bwd for callers that cannot allocate device memory
+ * when they run the backward (for example a plugin inside a framework that
+ * owns all device memory and gives it no allocator, or a real-time caller
+ * whose device-memory budget is fixed at start-up).  The source pages have no
+ * counterpart: this is a convenience of this library.
+ *
+ * Same arguments as attn_bwd minus the workspace: the scratch is a 32 MiB
+ * array compiled into the library, which every GPU that loads the library
+ * keeps until the process exits.  Problems whose attn_bwd_workspace_bytes()
+ * exceeds 32 MiB (about 64 K (query row, head) pairs at D = 128) are rejected
+ * with ATTN_E_TOO_LARGE.  Nothing is allocated or freed by the call.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make it before any stream capture.
+ * All calls on one device share the array: calls whose work overlaps on the
+ * GPU (unordered streams) race on it; order them.  The part that must start
+ * at zero is zero-filled on `stream` by every call.
+ */
+int attn_bwd_noalloc(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t* v,
+                     const attn_tensor_t* out, const attn_tensor_t* dout, const attn_tensor_t* lse,
+                     const attn_tensor_t* mask, const attn_tensor_t* cu_seqlens, int32_t max_seqlen,
+                     int causal, float scale, attn_tensor_t* dq, attn_tensor_t* dk,
+                     attn_tensor_t* dv, uint32_t flags, attn_stream_t stream);
 
 /*
  * attn_get_error - synchronises `stream`, then returns and clears the error

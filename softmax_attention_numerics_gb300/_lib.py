@@ -13,11 +13,11 @@ ATTN_EAGER_RESCALE = 2
 ERRORS = {
     0: "ATTN_OK", -1: "ATTN_E_DTYPE", -2: "ATTN_E_SHAPE", -3: "ATTN_E_LAYOUT",
     -4: "ATTN_E_DEVICE", -5: "ATTN_E_UNSUPPORTED", -6: "ATTN_E_WORKSPACE",
-    -7: "ATTN_E_CUDA", -8: "ATTN_E_TIMEOUT", -9: "ATTN_E_SEQLENS", -10: "ATTN_E_ARG", -11: "ATTN_E_INTERNAL",
+    -7: "ATTN_E_CUDA", -8: "ATTN_E_TIMEOUT", -9: "ATTN_E_SEQLENS", -10: "ATTN_E_ARG", -11: "ATTN_E_INTERNAL", -12: "ATTN_E_TOO_LARGE",
 }
 
 # Every symbol the header declares.
-EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_error",
+EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_bytes", "attn_get_error",
            "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_profile_events",
            "attn_launch_count")
 
@@ -62,6 +62,9 @@ def load():
     lib.attn_bwd.argtypes = [PT, PT, PT, PT, PT, PT, PT, PT, ctypes.c_int32, ctypes.c_int,
                              ctypes.c_float, PT, PT, PT, ctypes.c_void_p, ctypes.c_size_t,
                              ctypes.c_uint32, ctypes.c_void_p]
+    lib.attn_bwd_noalloc.restype = ctypes.c_int
+    lib.attn_bwd_noalloc.argtypes = [PT, PT, PT, PT, PT, PT, PT, PT, ctypes.c_int32, ctypes.c_int,
+                                     ctypes.c_float, PT, PT, PT, ctypes.c_uint32, ctypes.c_void_p]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_workspace_bytes.argtypes = [PT, PT, ctypes.c_uint32]
     lib.attn_get_error.restype = ctypes.c_int

@@ -450,6 +450,8 @@ extern "C" const char* attn_strerror(int code) {
         case ATTN_E_SEQLENS: return "cu_seqlens malformed or a sequence exceeds max_seqlen";
         case ATTN_E_ARG: return "null pointer or non-finite scale";
         case ATTN_E_INTERNAL: return "an internal invariant failed on the device";
+        case ATTN_E_TOO_LARGE:
+            return "problem needs more scratch than attn_bwd_noalloc's built-in 32 MiB array";
         default: return "unknown error code";
     }
 }

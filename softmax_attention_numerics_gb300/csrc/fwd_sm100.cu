@@ -6,7 +6,7 @@
 //   warp  8     TMA producer: Q tiles once, then K_j, V_j through a ring
 //   warp  9     TMEM allocator and single-thread UMMA issuer
 // TMEM (512 columns): S0 | S1 (128 fp32 columns each; the bf16 P of a tile is
-// written over the upper half of its S) | O0 | O1 (D columns each).
+// written over the first 64 columns of its S) | O0 | O1 (D columns each).
 //
 // Per key tile j the issuer runs, for t = 0, 1:
 //     O_t += P_t(j) V_j      (P from TMEM, V from shared memory)
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const uint32_t va = sbase + L::kKV + s * L::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
-                    mma_ts(tmem + colO[t], tmem + colS[t] + 64 + kk * 8,
+                    mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8,
                            smem_desc(va + kk * 2048, 16384, 1024, kSwizzle128B), idesc_pv,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -253,27 +253,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 break;
             }
             tc_fence_after();
-            float x[kTile];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, reinterpret_cast<uint32_t*>(x) + 32 * c);
-            tmem_wait_ld();
-
+            // Two passes over S in TMEM keep the register footprint small:
+            // pass 1 finds the tile max, pass 2 re-reads S and writes P over
+            // columns [0, 64) of S (P(keys 0-63) replaces S(keys 0-31) only
+            // after those were re-read).
             const int n0 = j * kTile;
             const bool pred = (n0 + kTile > si.len_k) ||
                               (p.causal && n0 + kTile - 1 > r0_tile) ||
                               (p.mask_kind != MASK_NONE);
+            const bool fast = !pred && p.scale_log2 > 0.f;
             float mt = -INFINITY;
-            if (pred) {
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t sv[64];
+                tmem_ld64(tS + 64 * hh, sv);
+                if (fast) {
+                    float mr = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < kTile; ++c) {
-                    x[c] = logit_log2(p, x[c], b, h, i, n0 + c, si.len_q, si.len_k);
-                    mt = fmaxf(mt, x[c]);
-                }
-            } else {
+                    for (int c = 0; c < 64; ++c) mr = fmaxf(mr, __uint_as_float(sv[c]));
+                    mt = fmaxf(mt, mr * p.scale_log2);
+                } else {
 #pragma unroll
-                for (int c = 0; c < kTile; ++c) {
-                    x[c] *= p.scale_log2;
-                    mt = fmaxf(mt, x[c]);
+                    for (int c = 0; c < 64; ++c) {
+                        const float xv = pred ? logit_log2(p, __uint_as_float(sv[c]), b, h, i,
+                                                           n0 + 64 * hh + c, si.len_q, si.len_k)
+                                              : __uint_as_float(sv[c]) * p.scale_log2;
+                        mt = fmaxf(mt, xv);
+                    }
                 }
             }
             // Online max: always m_new = max(m_ref, m_tile); lazy threshold 8.
@@ -297,18 +303,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 m_ref = m_new;
             }
             const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t sv[64];
+                tmem_ld64(tS + 64 * hh, sv);
+                uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2(fminf(x[32 * c + 2 * e] - ms, kLazyTau));
-                    const float p1 = ex2(fminf(x[32 * c + 2 * e + 1] - ms, kLazyTau));
+                for (int e = 0; e < 32; ++e) {
+                    float x0, x1;
+                    if (!pred) {
+                        x0 = __uint_as_float(sv[2 * e]) * p.scale_log2;
+                        x1 = __uint_as_float(sv[2 * e + 1]) * p.scale_log2;
+                    } else {
+                        x0 = logit_log2(p, __uint_as_float(sv[2 * e]), b, h, i, n0 + 64 * hh + 2 * e,
+                                        si.len_q, si.len_k);
+                        x1 = logit_log2(p, __uint_as_float(sv[2 * e + 1]), b, h, i,
+                                        n0 + 64 * hh + 2 * e + 1, si.len_q, si.len_k);
+                    }
+                    const float p0 = ex2(fminf(x0 - ms, kLazyTau));
+                    const float p1 = ex2(fminf(x1 - ms, kLazyTau));
                     l += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                     lr += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
                 }
-                tmem_st16(tS + 64 + 16 * c, pk);
+                tmem_st32(tS + 32 * hh, pk);
             }
             // Rescale O_t in TMEM (its previous MMA has completed: the commit that
             // signalled S_t(j) was issued after it).
