@@ -132,9 +132,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
+    // Each CTA starts its walk at a different (head, query tile): CTAs that run
+    // at the same time then reduce into different dQ rows instead of all
+    // hammering the same L2 lines.
+    const int rot = n_iter > 0 ? static_cast<int>(blockIdx.x % n_iter) : 0;
     auto iter_tile = [&](int it, int* h, int* m0) {
-        const int gi = it / per_head;
-        *m0 = (mt_first + it % per_head) * kT;
+        int itr = it + rot;
+        if (itr >= n_iter) itr -= n_iter;
+        const int gi = itr / per_head;
+        *m0 = (mt_first + itr % per_head) * kT;
         *h = hk * p.G + gi;
     };
 
@@ -200,6 +206,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             constexpr uint32_t id_dq = idesc_bf16(128, 64, 1, 1);      // dQ halves
             const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP;
             const uint32_t tDV = tmem + L::kColDV, tDK = tmem + L::kColDK;
+            const uint64_t k_k = smem_desc(sbase + L::kK, 16, 1024, kSwizzle128B);
+            const uint64_t v_k = smem_desc(sbase + L::kV, 16, 1024, kSwizzle128B);
+            const uint64_t k_mn = smem_desc(sbase + L::kK, 16384, 1024, kSwizzle128B);
+            const uint64_t ds_mn = smem_desc(sbase + L::kDS, 16384, 1024, kSwizzle128B);
             bool ok = mbar_wait(bar(L::kBarKV), 0, abort_flag);
             for (int it = 0; ok && it < n_iter; ++it) {
                 const int s = it & 1, r = it >> 1;
@@ -210,18 +220,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 tc_fence_after();
                 const uint32_t qa = sbase + L::kQ + s * L::kTileBytes;
                 const uint32_t da = sbase + L::kDO + s * L::kTileBytes;
+                const uint64_t q_k = smem_desc(qa, 16, 1024, kSwizzle128B);      // K-major
+                const uint64_t do_k = smem_desc(da, 16, 1024, kSwizzle128B);
+                const uint64_t q_mn = smem_desc(qa, 16384, 1024, kSwizzle128B);  // MN-major
+                const uint64_t do_mn = smem_desc(da, 16384, 1024, kSwizzle128B);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tS, smem_desc(sbase + L::kK + off, 16, 1024, kSwizzle128B),
-                           smem_desc(qa + off, 16, 1024, kSwizzle128B), id_kmaj, kk > 0);
+                    mma_ss(tS, desc_add(k_k, off), desc_add(q_k, off), id_kmaj, kk > 0);
                 }
                 mma_commit(bar(L::kBarS));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tDP, smem_desc(sbase + L::kV + off, 16, 1024, kSwizzle128B),
-                           smem_desc(da + off, 16, 1024, kSwizzle128B), id_kmaj, kk > 0);
+                    mma_ss(tDP, desc_add(v_k, off), desc_add(do_k, off), id_kmaj, kk > 0);
                 }
                 mma_commit(bar(L::kBarDP));
                 if (!(ok = mbar_wait(bar(L::kBarP), it & 1, abort_flag))) break;
@@ -229,10 +241,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk) {
                     const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tDV, tS + kk * 8, smem_desc(da + kk * 2048, 16384, 1024, kSwizzle128B),
-                           id_acc, acc);
-                    mma_ts(tDK, tDP + kk * 8, smem_desc(qa + kk * 2048, 16384, 1024, kSwizzle128B),
-                           id_acc, acc);
+                    mma_ts(tDV, tS + kk * 8, desc_add(do_mn, kk * 2048), id_acc, acc);
+                    mma_ts(tDK, tDP + kk * 8, desc_add(q_mn, kk * 2048), id_acc, acc);
                 }
                 mma_commit(bar(L::kBarQEmpty + s));
                 if (with_dq) {
@@ -241,10 +251,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                         const uint32_t dst = (hh == 0 ? tS : tDP) + 64;
 #pragma unroll
                         for (int kk = 0; kk < kT / 16; ++kk)
-                            mma_ss(dst, smem_desc(sbase + L::kDS + kk * 2048, 16384, 1024, kSwizzle128B),
-                                   smem_desc(sbase + L::kK + hh * 16384 + kk * 2048, 16384, 1024,
-                                             kSwizzle128B),
-                                   id_dq, kk > 0);
+                            mma_ss(dst, desc_add(ds_mn, kk * 2048),
+                                   desc_add(k_mn, hh * 16384 + kk * 2048), id_dq, kk > 0);
                     }
                 }
                 mma_commit(bar(L::kBarDQFull));
@@ -288,23 +296,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 uint32_t sv[32], dv[32];
                 tmem_ld32(tS + 32 * c, sv);
                 tmem_ld32(tDP + 32 * c, dv);
+                // lse2 / Delta of this chunk's 32 query rows: 16 independent
+                // 16-byte shared loads (every lane reads the same address).
+                float lv[32], dl[32];
+                const uint32_t va = smem_u32(lse2 + 32 * c);
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4) {
+                    const float4 a = lds128(va + 16 * v4);
+                    const float4 d = lds128(va + 512 + 16 * v4);
+                    lv[4 * v4] = a.x; lv[4 * v4 + 1] = a.y; lv[4 * v4 + 2] = a.z; lv[4 * v4 + 3] = a.w;
+                    dl[4 * v4] = d.x; dl[4 * v4 + 1] = d.y; dl[4 * v4 + 2] = d.z; dl[4 * v4 + 3] = d.w;
+                }
                 uint32_t pk[16], dk[16];
+                if (!pred) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pr[2], ds[2];
+                    for (int e = 0; e < 32; e += 2) {
+                        float pr[2], ds[2];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int q = 32 * c + e + u;
-                        const float acc = __uint_as_float(sv[e + u]);
-                        const float x = pred ? logit_log2(p, acc, b, h, m0 + q, j, si.len_q, si.len_k)
-                                             : acc * p.scale_log2;
-                        const bool vis = x != -INFINITY;
-                        const float pv = ex2(fminf(x - lse2[q], 0.f));
-                        pr[u] = vis ? pv : 0.f;
-                        ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - del[q]) : 0.f;
+                        for (int u = 0; u < 2; ++u) {
+                            const float x = __uint_as_float(sv[e + u]) * p.scale_log2;
+                            pr[u] = ex2(fminf(x - lv[e + u], 0.f));
+                            ds[u] = pr[u] * (__uint_as_float(dv[e + u]) - dl[e + u]);
+                        }
+                        pk[e >> 1] = pack_bf16(pr[0], pr[1]);
+                        dk[e >> 1] = pack_bf16(ds[0], ds[1]);
                     }
-                    pk[e >> 1] = pack_bf16(pr[0], pr[1]);
-                    dk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float pr[2], ds[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int q = 32 * c + e + u;
+                            const float x = logit_log2(p, __uint_as_float(sv[e + u]), b, h, m0 + q, j,
+                                                       si.len_q, si.len_k);
+                            const bool vis = x != -INFINITY;
+                            const float pv = ex2(fminf(x - lv[e + u], 0.f));
+                            pr[u] = vis ? pv : 0.f;
+                            ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dl[e + u]) : 0.f;
+                        }
+                        pk[e >> 1] = pack_bf16(pr[0], pr[1]);
+                        dk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                    }
                 }
                 tmem_st16(tS + 16 * c, pk);
                 tmem_st16(tDP + 16 * c, dk);

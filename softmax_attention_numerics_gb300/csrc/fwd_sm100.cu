@@ -164,22 +164,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             auto kv_par = [&](int li) { return (uint32_t)((li / L::kStages) & 1); };
             auto issue_qk = [&](int t, int j) {
                 const int s = kv_stage(2 * j);
-                const uint32_t qa = sbase + L::kQ + t * L::kTileBytes;
-                const uint32_t ka = sbase + L::kKV + s * L::kTileBytes;
+                const uint64_t qd = smem_desc(sbase + L::kQ + t * L::kTileBytes, 16, 1024, kSwizzle128B);
+                const uint64_t kd = smem_desc(sbase + L::kKV + s * L::kTileBytes, 16, 1024, kSwizzle128B);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem + colS[t], smem_desc(qa + off, 16, 1024, kSwizzle128B),
-                           smem_desc(ka + off, 16, 1024, kSwizzle128B), idesc_qk, kk > 0);
+                    mma_ss(tmem + colS[t], desc_add(qd, off), desc_add(kd, off), idesc_qk, kk > 0);
                 }
             };
             auto issue_pv = [&](int t, int j) {
                 const int s = kv_stage(2 * j + 1);
-                const uint32_t va = sbase + L::kKV + s * L::kTileBytes;
+                const uint64_t vd = smem_desc(sbase + L::kKV + s * L::kTileBytes, 16384, 1024, kSwizzle128B);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
-                    mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8,
-                           smem_desc(va + kk * 2048, 16384, 1024, kSwizzle128B), idesc_pv,
+                    mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8, desc_add(vd, kk * 2048), idesc_pv,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };

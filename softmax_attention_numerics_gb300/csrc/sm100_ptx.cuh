@@ -125,6 +125,15 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                  : "memory");
 }
 
+// 16-byte shared-memory load from a 32-bit shared address.
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -247,6 +256,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
     d |= 1ull << 46;
     d |= swz << 61;
     return d;
+}
+
+// Descriptor of the same matrix advanced by `bytes` (a multiple of 16): the
+// start-address field holds addr >> 4 and shared addresses stay below 2^18,
+// so the addition never carries out of the field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+    return d + static_cast<uint64_t>(bytes >> 4);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulate.
