@@ -292,10 +292,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             const bool pred = (n0 + kT > si.len_k) || (m0 + kT > si.len_q) ||
                               (p.causal && n0 + kT - 1 > m0) || (p.mask_kind != MASK_NONE);
 #pragma unroll
+            if (p.mask_kind != MASK_NONE) {
+                // With a user mask, rewrite S^T in TMEM as finished logits chunk by
+                // chunk first (mask loads in the main loop would spill registers).
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tS + 32 * c, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = __float_as_uint(logit_log2(p, __uint_as_float(v[e]), b, h,
+                                                          m0 + 32 * c + e, j, si.len_q, si.len_k));
+                    tmem_st32(tS + 32 * c, v);
+                }
+                tmem_wait_st();
+            }
             for (int c = 0; c < 4; ++c) {
                 uint32_t sv[32], dv[32];
-                tmem_ld32(tS + 32 * c, sv);
-                tmem_ld32(tDP + 32 * c, dv);
+                tmem_ld32x2(tS + 32 * c, sv, tDP + 32 * c, dv);
                 // lse2 / Delta of this chunk's 32 query rows: 16 independent
                 // 16-byte shared loads (every lane reads the same address).
                 float lv[32], dl[32];
@@ -308,7 +322,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                     dl[4 * v4] = d.x; dl[4 * v4 + 1] = d.y; dl[4 * v4 + 2] = d.z; dl[4 * v4 + 3] = d.w;
                 }
                 uint32_t pk[16], dk[16];
-                if (!pred) {
+                if (!pred && p.mask_kind == MASK_NONE) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float pr[2], ds[2];
@@ -321,15 +335,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                         pk[e >> 1] = pack_bf16(pr[0], pr[1]);
                         dk[e >> 1] = pack_bf16(ds[0], ds[1]);
                     }
-                } else {
+                } else if (p.mask_kind == MASK_NONE) {
+                    // keys past the sequence, query rows past it, causal pairs
+                    const int qlo = p.causal ? j - m0 : -1;          // visible: q >= qlo
+                    const int qhi = (j < si.len_k) ? si.len_q - m0 : 0;  // visible: q < qhi
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float pr[2], ds[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             const int q = 32 * c + e + u;
-                            const float x = logit_log2(p, __uint_as_float(sv[e + u]), b, h, m0 + q, j,
-                                                       si.len_q, si.len_k);
+                            const bool vis = q >= qlo && q < qhi;
+                            const float x = __uint_as_float(sv[e + u]) * p.scale_log2;
+                            const float pv = ex2(fminf(x - lv[e + u], 0.f));
+                            pr[u] = vis ? pv : 0.f;
+                            ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dl[e + u]) : 0.f;
+                        }
+                        pk[e >> 1] = pack_bf16(pr[0], pr[1]);
+                        dk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                    }
+                } else {
+                    // mask: S^T already holds the finished log2-domain logits
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float pr[2], ds[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const float x = __uint_as_float(sv[e + u]);
                             const bool vis = x != -INFINITY;
                             const float pv = ex2(fminf(x - lv[e + u], 0.f));
                             pr[u] = vis ? pv : 0.f;
@@ -413,8 +445,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
 #pragma unroll
                 for (int hh = 0; hh < L::kBlocks; ++hh) {
                     const uint32_t src = tmem + lane_off + (hh == 0 ? L::kColS : L::kColDP) + 64;
-                    tmem_ld32(src, reinterpret_cast<uint32_t*>(dq) + 64 * hh);
-                    tmem_ld32(src + 32, reinterpret_cast<uint32_t*>(dq) + 64 * hh + 32);
+                    tmem_ld32x2(src, reinterpret_cast<uint32_t*>(dq) + 64 * hh, src + 32,
+                                reinterpret_cast<uint32_t*>(dq) + 64 * hh + 32);
                 }
             }
             tc_fence_before();

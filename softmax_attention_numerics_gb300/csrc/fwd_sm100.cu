@@ -251,33 +251,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 break;
             }
             tc_fence_after();
-            // Two passes over S in TMEM keep the register footprint small:
-            // pass 1 finds the tile max, pass 2 re-reads S and writes P over
-            // columns [0, 64) of S (P(keys 0-63) replaces S(keys 0-31) only
-            // after those were re-read).
+            // The whole row of S comes to registers with one TMEM load; P is
+            // then written over S columns [0, 64).  With a user mask the
+            // logits are first rewritten in TMEM chunk by chunk (the mask
+            // loads would otherwise hold too many registers).
             const int n0 = j * kTile;
-            const bool pred = (n0 + kTile > si.len_k) ||
-                              (p.causal && n0 + kTile - 1 > r0_tile) ||
-                              (p.mask_kind != MASK_NONE);
-            const bool fast = !pred && p.scale_log2 > 0.f;
+            const bool has_mask = p.mask_kind != MASK_NONE;
+            const bool pred = (n0 + kTile > si.len_k) || (p.causal && n0 + kTile - 1 > r0_tile);
+            float x[kTile];
             float mt = -INFINITY;
+            if (has_mask) {
 #pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t sv[64];
-                tmem_ld64(tS + 64 * hh, sv);
-                if (fast) {
-                    float mr = -INFINITY;
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tS + 32 * c, v);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) mr = fmaxf(mr, __uint_as_float(sv[c]));
-                    mt = fmaxf(mt, mr * p.scale_log2);
-                } else {
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = __float_as_uint(logit_log2(p, __uint_as_float(v[e]), b, h, i,
+                                                          n0 + 32 * c + e, si.len_q, si.len_k));
+                    tmem_st32(tS + 32 * c, v);
+                }
+                tmem_wait_st();
+                tmem_ld128(tS, reinterpret_cast<uint32_t*>(x));
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const float xv = pred ? logit_log2(p, __uint_as_float(sv[c]), b, h, i,
-                                                           n0 + 64 * hh + c, si.len_q, si.len_k)
-                                              : __uint_as_float(sv[c]) * p.scale_log2;
-                        mt = fmaxf(mt, xv);
-                    }
+                for (int c = 0; c < kTile; ++c) mt = fmaxf(mt, x[c]);
+            } else if (pred) {
+                tmem_ld128(tS, reinterpret_cast<uint32_t*>(x));
+                const int jmax = p.causal ? min(si.len_k, i + 1) : si.len_k;   // keys < jmax visible
+                const bool row_in = i < si.len_q;
+#pragma unroll
+                for (int c = 0; c < kTile; ++c) {
+                    x[c] = (row_in && n0 + c < jmax) ? x[c] * p.scale_log2 : -INFINITY;
+                    mt = fmaxf(mt, x[c]);
+                }
+            } else {
+                tmem_ld128(tS, reinterpret_cast<uint32_t*>(x));
+#pragma unroll
+                for (int c = 0; c < kTile; ++c) {
+                    x[c] *= p.scale_log2;
+                    mt = fmaxf(mt, x[c]);
                 }
             }
             // Online max: always m_new = max(m_ref, m_tile); lazy threshold 8.
@@ -301,30 +313,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 m_ref = m_new;
             }
             const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
-#pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t sv[64];
-                tmem_ld64(tS + 64 * hh, sv);
-                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float x0, x1;
-                    if (!pred) {
-                        x0 = __uint_as_float(sv[2 * e]) * p.scale_log2;
-                        x1 = __uint_as_float(sv[2 * e + 1]) * p.scale_log2;
-                    } else {
-                        x0 = logit_log2(p, __uint_as_float(sv[2 * e]), b, h, i, n0 + 64 * hh + 2 * e,
-                                        si.len_q, si.len_k);
-                        x1 = logit_log2(p, __uint_as_float(sv[2 * e + 1]), b, h, i,
-                                        n0 + 64 * hh + 2 * e + 1, si.len_q, si.len_k);
-                    }
-                    const float p0 = ex2(fminf(x0 - ms, kLazyTau));
-                    const float p1 = ex2(fminf(x1 - ms, kLazyTau));
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ex2(fminf(x[32 * c + 2 * e] - ms, kLazyTau));
+                    const float p1 = ex2(fminf(x[32 * c + 2 * e + 1] - ms, kLazyTau));
                     l += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                     lr += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
                 }
-                tmem_st32(tS + 32 * hh, pk);
+                tmem_st16(tS + 16 * c, pk);
             }
             // Rescale O_t in TMEM (its previous MMA has completed: the commit that
             // signalled S_t(j) was issued after it).
@@ -333,7 +333,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
                     tmem_ld32(tO + 32 * c, o);
-                    tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
