@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 const int i = m0 + q;
                 const int64_t li = b * p.lse_b + h * p.lse_h + row_base + i;
                 const bool in = i < si.len_q;
-                vec[s * 256 + q] = in ? p.lse2[li] : 0.f;
+                vec[s * 256 + q] = in ? -p.lse2[li] : 0.f;     // stored negated
                 vec[s * 256 + 128 + q] = in ? p.delta[li] : 0.f;
             }
             mbar_arrive(bar(L::kBarQFull + s));
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             for (int c = 0; c < 4; ++c) {
                 uint32_t sv[32], dv[32];
                 tmem_ld32x2(tS + 32 * c, sv, tDP + 32 * c, dv);
-                // lse2 / Delta of this chunk's 32 query rows: 16 independent
+                // -lse2 / Delta of this chunk's 32 query rows: 16 independent
                 // 16-byte shared loads (every lane reads the same address).
                 float lv[32], dl[32];
                 const uint32_t va = smem_u32(lse2 + 32 * c);
@@ -323,17 +323,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 }
                 uint32_t pk[16], dk[16];
                 if (!pred && p.mask_kind == MASK_NONE) {
+                    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        float pr[2], ds[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const float x = __uint_as_float(sv[e + u]) * p.scale_log2;
-                            pr[u] = ex2(fminf(x - lv[e + u], 0.f));
-                            ds[u] = pr[u] * (__uint_as_float(dv[e + u]) - dl[e + u]);
-                        }
-                        pk[e >> 1] = pack_bf16(pr[0], pr[1]);
-                        dk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                        // packed pairs: x - lse2 = s*c + (-lse2); dP - Delta; P*(dP - Delta)
+                        const float2 x2 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                c2, make_float2(lv[e], lv[e + 1]));
+                        const float p0 = ex2(fminf(x2.x, 0.f));
+                        const float p1 = ex2(fminf(x2.y, 0.f));
+                        const float2 d2 = fadd2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                                make_float2(-dl[e], -dl[e + 1]));
+                        const float2 ds2 = fmul2(make_float2(p0, p1), d2);
+                        pk[e >> 1] = pack_bf16(p0, p1);
+                        dk[e >> 1] = pack_bf16(ds2.x, ds2.y);
                     }
                 } else if (p.mask_kind == MASK_NONE) {
                     // keys past the sequence, query rows past it, causal pairs
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                             const int q = 32 * c + e + u;
                             const bool vis = q >= qlo && q < qhi;
                             const float x = __uint_as_float(sv[e + u]) * p.scale_log2;
-                            const float pv = ex2(fminf(x - lv[e + u], 0.f));
+                            const float pv = ex2(fminf(x + lv[e + u], 0.f));
                             pr[u] = vis ? pv : 0.f;
                             ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dl[e + u]) : 0.f;
                         }
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                         for (int u = 0; u < 2; ++u) {
                             const float x = __uint_as_float(sv[e + u]);
                             const bool vis = x != -INFINITY;
-                            const float pv = ex2(fminf(x - lv[e + u], 0.f));
+                            const float pv = ex2(fminf(x + lv[e + u], 0.f));
                             pr[u] = vis ? pv : 0.f;
                             ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dl[e + u]) : 0.f;
                         }
