@@ -53,14 +53,13 @@ struct BwdLayout {
     static constexpr int kBarKV = 0;
     static constexpr int kBarQFull = 1;                 // [2]
     static constexpr int kBarQEmpty = 3;                // [2]
-    static constexpr int kBarS = 5;
-    static constexpr int kBarDP = 6;
-    static constexpr int kBarP = 7;
-    static constexpr int kBarDQFull = 8;
-    static constexpr int kBarDQRead = 9;
-    static constexpr int kBarAcc = 10;
-    static constexpr int kBarDrain = 11;
-    static constexpr int kNumBars = 12;
+    static constexpr int kBarSdp = 5;      // [2]: S^T and dP^T of query half 0 / 1 done
+    static constexpr int kBarP = 7;        // [2]: P^T, dS^T of query half 0 / 1 written
+    static constexpr int kBarDQFull = 9;
+    static constexpr int kBarDQRead = 10;
+    static constexpr int kBarAcc = 11;
+    static constexpr int kBarDrain = 12;
+    static constexpr int kNumBars = 13;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     static constexpr uint32_t kTmemCols = 512;
@@ -116,7 +115,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
         for (int i = 0; i < L::kNumBars; ++i) {
             uint32_t cnt = 1;
             if (i == L::kBarQFull || i == L::kBarQFull + 1) cnt = 33;
-            if (i == L::kBarP || i == L::kBarDQRead) cnt = kT;
+            if (i == L::kBarP || i == L::kBarP + 1 || i == L::kBarDQRead) cnt = kT;
             mbar_init(bar(i), cnt);
         }
         *abort_flag = 0;
@@ -201,7 +200,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
     } else if (warp == 9) {
         // ------------------------------------------------------------ UMMA issuer
         if (lane == 0) {
-            constexpr uint32_t id_kmaj = idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
+            constexpr uint32_t id_half = idesc_bf16(128, 64, 0, 0);    // S^T, dP^T halves
             constexpr uint32_t id_acc = idesc_bf16(128, D, 0, 1);      // dV, dK (B MN-major)
             constexpr uint32_t id_dq = idesc_bf16(128, 64, 1, 1);      // dQ halves
             const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP;
@@ -224,26 +223,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 const uint64_t do_k = smem_desc(da, 16, 1024, kSwizzle128B);
                 const uint64_t q_mn = smem_desc(qa, 16384, 1024, kSwizzle128B);  // MN-major
                 const uint64_t do_mn = smem_desc(da, 16384, 1024, kSwizzle128B);
+                // S^T and dP^T in two query halves (N = 64) so that the compute
+                // warps start on half 0 while the tensor core produces half 1.
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tS, desc_add(k_k, off), desc_add(q_k, off), id_kmaj, kk > 0);
-                }
-                mma_commit(bar(L::kBarS));
+                for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tDP, desc_add(v_k, off), desc_add(do_k, off), id_kmaj, kk > 0);
-                }
-                mma_commit(bar(L::kBarDP));
-                if (!(ok = mbar_wait(bar(L::kBarP), it & 1, abort_flag))) break;
-                tc_fence_after();
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tS + 64 * hf, desc_add(k_k, off), desc_add(q_k, off + 8192 * hf),
+                               id_half, kk > 0);
+                    }
 #pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk) {
-                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tDV, tS + kk * 8, desc_add(do_mn, kk * 2048), id_acc, acc);
-                    mma_ts(tDK, tDP + kk * 8, desc_add(q_mn, kk * 2048), id_acc, acc);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tDP + 64 * hf, desc_add(v_k, off), desc_add(do_k, off + 8192 * hf),
+                               id_half, kk > 0);
+                    }
+                    mma_commit(bar(L::kBarSdp + hf));
                 }
+                // dV += P^T dO, dK += dS^T Q, one query half at a time as P^T and
+                // dS^T of that half arrive.
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    if (!(ok = mbar_wait(bar(L::kBarP + hf), it & 1, abort_flag))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq) {
+                        const int kk = 4 * hf + kq;
+                        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                        mma_ts(tDV, tS + kk * 8, desc_add(do_mn, kk * 2048), id_acc, acc);
+                        mma_ts(tDK, tDP + kk * 8, desc_add(q_mn, kk * 2048), id_acc, acc);
+                    }
+                }
+                if (!ok) break;
                 mma_commit(bar(L::kBarQEmpty + s));
                 if (with_dq) {
 #pragma unroll
@@ -278,25 +290,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             const int s = it & 1;
             int h, m0;
             iter_tile(it, &h, &m0);
+            const float* lse2 = vec + s * 256;
+            const bool pred = (n0 + kT > si.len_k) || (m0 + kT > si.len_q) ||
+                              (p.causal && n0 + kT - 1 > m0) || (p.mask_kind != MASK_NONE);
+            // Query half hf (columns 64 hf .. 64 hf + 63) as soon as its S^T, dP^T land.
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
             // q_full[s] also publishes the producer's lse2 / Delta vectors.
-            ok = mbar_wait(bar(L::kBarQFull + s), (it >> 1) & 1, abort_flag) &&
-                 mbar_wait(bar(L::kBarS), it & 1, abort_flag) &&
-                 mbar_wait(bar(L::kBarDP), it & 1, abort_flag);
+            ok = (hf > 0 || mbar_wait(bar(L::kBarQFull + s), (it >> 1) & 1, abort_flag)) &&
+                 mbar_wait(bar(L::kBarSdp + hf), it & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float* lse2 = vec + s * 256;
-            const float* del = lse2 + 128;
-            const bool pred = (n0 + kT > si.len_k) || (m0 + kT > si.len_q) ||
-                              (p.causal && n0 + kT - 1 > m0) || (p.mask_kind != MASK_NONE);
-#pragma unroll
             if (p.mask_kind != MASK_NONE) {
-                // With a user mask, rewrite S^T in TMEM as finished logits chunk by
-                // chunk first (mask loads in the main loop would spill registers).
+                // With a user mask, rewrite this half of S^T in TMEM as finished
+                // logits first (mask loads in the main loop would spill registers).
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * hf + cc;
                     uint32_t v[32];
                     tmem_ld32(tS + 32 * c, v);
 #pragma unroll
@@ -307,7 +320,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 }
                 tmem_wait_st();
             }
-            for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * hf + cc;
                 uint32_t sv[32], dv[32];
                 tmem_ld32x2(tS + 32 * c, sv, tDP + 32 * c, dv);
                 // -lse2 / Delta of this chunk's 32 query rows: 16 independent
@@ -380,7 +395,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             tmem_wait_st();
             fence_proxy_async_smem();      // dS in shared memory -> the dQ MMA
             tc_fence_before();
-            mbar_arrive(bar(L::kBarP));
+            mbar_arrive(bar(L::kBarP + hf));
+            }
+            if (!ok) break;
         }
         // dV epilogue: staging tile = the dS buffer (free once every MMA is done).
         if (ok) {
