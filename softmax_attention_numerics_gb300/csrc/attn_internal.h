@@ -71,6 +71,10 @@ constexpr int DEV_E_INTERNAL = -11;
 bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t S, int64_t B,
                    int64_t sh, int64_t ss, int64_t sb);
 
+// TMA tensor map over the fp32 dQ workspace [R, H, D] (dims D, H, R), box
+// 32 x 1 x 128, 128-byte swizzle; the target of bulk reduce-adds.
+bool make_f32_reduce_map(CUtensorMap* m, void* base, int64_t D, int64_t H, int64_t R);
+
 // Launchers (each enqueues on `stream`, returns cudaGetLastError()).
 cudaError_t launch_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const Problem& p, cudaStream_t stream);

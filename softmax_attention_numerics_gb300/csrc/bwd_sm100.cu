@@ -67,7 +67,7 @@ struct BwdLayout {
 };
 
 struct BwdMaps {
-    CUtensorMap k, v, q, dout, dk, dv;
+    CUtensorMap k, v, q, dout, dk, dv, dq_acc;
 };
 
 // Write one 32-column chunk of a row into a TMA-layout staging tile
@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
         for (int i = 0; i < L::kNumBars; ++i) {
             uint32_t cnt = 1;
             if (i == L::kBarQFull || i == L::kBarQFull + 1) cnt = 33;
+            // q_empty: the MMAs' commit + the dQ warps once their reduction read the stage
+            if (i == L::kBarQEmpty || i == L::kBarQEmpty + 1) cnt = 2;
             if (i == L::kBarP || i == L::kBarP + 1 || i == L::kBarDQRead) cnt = kT;
             mbar_init(bar(i), cnt);
         }
@@ -135,6 +137,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
     // at the same time then reduce into different dQ rows instead of all
     // hammering the same L2 lines.
     const int rot = n_iter > 0 ? static_cast<int>(blockIdx.x % n_iter) : 0;
+    // Byte offset of fp32 dQ staging block `blk` inside query/dO stage `s`.
+    auto dq_stage_off = [&](int blk, int s) {
+        return ((blk & 1) ? L::kDO : L::kQ) + s * L::kTileBytes + (blk >> 1) * 16384;
+    };
     auto iter_tile = [&](int it, int* h, int* m0) {
         int itr = it + rot;
         if (itr >= n_iter) itr -= n_iter;
@@ -404,14 +410,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             ok = mbar_wait(bar(L::kBarAcc), 0, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
-        if (ok) {
-            tc_fence_after();
+        {
+            if (ok) tc_fence_after();
             const bool tma_path = !p.varlen || n0 + kT <= si.len_k;
             bf16* grow = p.dv + b * p.dk_b + static_cast<int64_t>(row_base + j) * p.dk_s + hk * p.dk_h;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                if (n_iter > 0) {
+                if (ok && n_iter > 0) {
                     tmem_ld32(tmem + lane_off + L::kColDV + 32 * c, o);
                 } else {
 #pragma unroll
@@ -421,7 +427,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     pk[e] = pack_bf16(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
-                if (tma_path) {
+                if (!ok) {
+                } else if (tma_path) {
                     stage_row_chunk(ds_tile, r, 32 * c, pk);
                 } else if (j < si.len_k) {
                     uint4* dst = reinterpret_cast<uint4*>(grow + 32 * c);
@@ -431,9 +438,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 }
             }
             if (tma_path) {
-                fence_proxy_async_smem();   // each writer: its stores -> async proxy
-                named_bar_sync(1, 128);     // all 128 rows are in the staging tile
-                if (r == 0) {
+                if (ok) fence_proxy_async_smem();   // each writer: its stores -> async proxy
+                named_bar_sync(1, 128);             // all 128 rows are in the staging tile
+                if (ok && r == 0) {
 #pragma unroll
                     for (int c = 0; c < L::kBlocks; ++c)
                         tma_store_4d(&maps.dv, sbase + L::kDS + c * 16384, 64 * c, hk, row_base + n0,
@@ -453,39 +460,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
         for (int it = 0; it < n_iter; ++it) {
             int h, m0;
             iter_tile(it, &h, &m0);
-            ok = mbar_wait(bar(L::kBarDQFull), it & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
+            // After a wait gives up, `ok` stays false: the warp skips the work but
+            // still meets every named barrier, so none is left short.
+            if (ok) {
+                ok = mbar_wait(bar(L::kBarDQFull), it & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
             }
-            tc_fence_after();
             float dq[D];
-            if (with_dq) {
+            if (ok) {
+                tc_fence_after();
+                if (with_dq) {
 #pragma unroll
-                for (int hh = 0; hh < L::kBlocks; ++hh) {
-                    const uint32_t src = tmem + lane_off + (hh == 0 ? L::kColS : L::kColDP) + 64;
-                    tmem_ld32x2(src, reinterpret_cast<uint32_t*>(dq) + 64 * hh, src + 32,
-                                reinterpret_cast<uint32_t*>(dq) + 64 * hh + 32);
+                    for (int hh = 0; hh < L::kBlocks; ++hh) {
+                        const uint32_t src = tmem + lane_off + (hh == 0 ? L::kColS : L::kColDP) + 64;
+                        tmem_ld32x2(src, reinterpret_cast<uint32_t*>(dq) + 64 * hh, src + 32,
+                                    reinterpret_cast<uint32_t*>(dq) + 64 * hh + 32);
+                    }
                 }
+                tc_fence_before();
+                mbar_arrive(bar(L::kBarDQRead));
             }
-            tc_fence_before();
-            mbar_arrive(bar(L::kBarDQRead));
-            const int i = m0 + r;
-            if (with_dq && i < si.len_q) {
-                float* dst = p.dq_acc + (b * p.acc_b + row_base + i) * static_cast<int64_t>(p.Hq) * D +
-                             static_cast<int64_t>(h) * D;
+            // Reduce dQ_i into the fp32 workspace with bulk tensor reductions,
+            // staged in this tile's query/dO stage: every MMA that read it has
+            // completed (dq_full covers them), and the stage returns to the
+            // producer only once the reductions have read the staging.
+            const int s = it & 1;
+            if (with_dq) {
+                if (ok) {
+                    // fp32 staging: D/32 blocks of [128 rows][128 B], 16-byte chunks
+                    // swizzled; even blocks in the query stage, odd ones in the dO stage.
 #pragma unroll
-                for (int v = 0; v < D / 4; ++v)
-                    red_add_v4(dst + 4 * v, dq[4 * v], dq[4 * v + 1], dq[4 * v + 2], dq[4 * v + 3]);
+                    for (int blk = 0; blk < D / 32; ++blk) {
+                        uint8_t* base = smem + dq_stage_off(blk, s);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            float4* dst = reinterpret_cast<float4*>(base + r * 128 + ((k ^ (r & 7)) << 4));
+                            *dst = make_float4(dq[32 * blk + 4 * k], dq[32 * blk + 4 * k + 1],
+                                               dq[32 * blk + 4 * k + 2], dq[32 * blk + 4 * k + 3]);
+                        }
+                    }
+                    fence_proxy_async_smem();      // each writer: its stores -> async proxy
+                }
+                named_bar_sync(2, 128);            // the whole 128 x D tile is staged
+                if (ok && r == 0) {
+                    const int acc_row = static_cast<int>(b * p.acc_b) + row_base + m0;
+#pragma unroll
+                    for (int blk = 0; blk < D / 32; ++blk)
+                        tma_reduce_add_3d(&maps.dq_acc, sbase + dq_stage_off(blk, s), 32 * blk, h,
+                                          acc_row);
+                    bulk_commit();
+                    bulk_wait_read_all();          // only the committing thread may wait
+                    mbar_arrive(bar(L::kBarQEmpty + s));
+                }
+            } else if (ok && r == 0) {
+                mbar_arrive(bar(L::kBarQEmpty + s));
             }
         }
-        // dK epilogue: staging tile = query stage 0 (free once every MMA is done).
+        // dK epilogue: staging tile = query stage 0 (free once every MMA is done
+        // and the last dQ reduction has read it: its issuer waited for that
+        // before this barrier).
+        named_bar_sync(2, 128);
         if (ok) {
             ok = mbar_wait(bar(L::kBarAcc), 0, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
-        if (ok) {
-            tc_fence_after();
+        {
+            if (ok) tc_fence_after();
             const int j = n0 + r;
             uint8_t* tile = smem + L::kQ;
             const bool tma_path = !p.varlen || n0 + kT <= si.len_k;
@@ -493,7 +533,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                if (n_iter > 0) {
+                if (ok && n_iter > 0) {
                     tmem_ld32(tmem + lane_off + L::kColDK + 32 * c, o);
                 } else {
 #pragma unroll
@@ -504,7 +544,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 for (int e = 0; e < 16; ++e)
                     pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * p.scale,
                                       __uint_as_float(o[2 * e + 1]) * p.scale);
-                if (tma_path) {
+                if (!ok) {
+                } else if (tma_path) {
                     stage_row_chunk(tile, r, 32 * c, pk);
                 } else if (j < si.len_k) {
                     uint4* dst = reinterpret_cast<uint4*>(grow + 32 * c);
@@ -514,9 +555,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 }
             }
             if (tma_path) {
-                fence_proxy_async_smem();
+                if (ok) fence_proxy_async_smem();
                 named_bar_sync(2, 128);
-                if (r == 0) {
+                if (ok && r == 0) {
 #pragma unroll
                     for (int c = 0; c < L::kBlocks; ++c)
                         tma_store_4d(&maps.dk, sbase + L::kQ + c * 16384, 64 * c, hk, row_base + n0,
@@ -558,6 +599,12 @@ cudaError_t launch_bwd_sm100_d(const Problem& p, bool with_dq, cudaStream_t stre
                        no_q ? p.k_h : p.do_h, no_q ? p.k_s : p.do_s, no_q ? p.k_b : p.do_b) &&
               make_tile_map(&maps.dk, p.dk, D, p.Hkv, Sk, Bm, p.dk_h, p.dk_s, p.dk_b) &&
               make_tile_map(&maps.dv, p.dv, D, p.Hkv, Sk, Bm, p.dk_h, p.dk_s, p.dk_b);
+    if (with_dq) {
+        const int64_t rows = p.varlen ? p.T : static_cast<int64_t>(p.B) * p.Sq;
+        ok = ok && make_f32_reduce_map(&maps.dq_acc, p.dq_acc, D, p.Hq, rows);
+    } else {
+        maps.dq_acc = maps.k;   // never read without dQ
+    }
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(bwd_sm100_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);

@@ -44,4 +44,17 @@ bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64
            CUDA_SUCCESS;
 }
 
+bool make_f32_reduce_map(CUtensorMap* m, void* base, int64_t D, int64_t H, int64_t R) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(R > 0 ? R : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)(D * 4), (cuuint64_t)(H * D * 4)};
+    cuuint32_t box[3] = {32, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 }  // namespace attn
