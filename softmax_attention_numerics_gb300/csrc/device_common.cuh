@@ -1,5 +1,5 @@
 // Device helpers shared by the attention kernels: sequence bounds, mask and
-// predicate evaluation, shared-memory swizzle, and thin PTX wrappers.
+// predicate evaluation, exp2 / log2 and bf16 packing.
 #pragma once
 
 #include <math.h>
@@ -92,71 +92,9 @@ __device__ __forceinline__ float logit_log2(const Problem& p, float acc, int b, 
     return x;
 }
 
-// ---------------------------------------------------------------- cp.async
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool pred) {
-    const int sz = pred ? 16 : 0;   // 0 bytes read -> 16 zero bytes written
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-// Element offset of 16-byte chunk c of row r in a [rows][D] bf16 tile whose
-// chunks are XOR-swizzled by (r mod 8) (conflict-free ldmatrix).
-template <int D>
-__device__ __forceinline__ int swz(int r, int c) {
-    return r * D + ((c ^ (r & 7)) << 3);
-}
-
-// Copy rows [0, R) of a bf16 [*, D] matrix (row stride `rs` elements) into a
-// swizzled shared tile; rows >= rows_valid are zero-filled (never read).
-template <int R, int D, int NT>
-__device__ __forceinline__ void load_tile(bf16* s, const bf16* g, int64_t rs, int rows_valid,
-                                          const bf16* safe, int tid) {
-    constexpr int CH = D / 8;
-#pragma unroll
-    for (int idx = tid; idx < R * CH; idx += NT) {
-        const int r = idx / CH, c = idx % CH;
-        const bool ok = r < rows_valid;
-        const bf16* src = ok ? g + static_cast<int64_t>(r) * rs + c * 8 : safe;
-        cp_async_16(smem_u32(s + swz<D>(r, c)), src, ok);
-    }
-}
-
-// ---------------------------------------------------------------- mma.sync
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float bf16_round(float x) {
-    return __bfloat162float(__float2bfloat16_rn(x));
 }
 
 }  // namespace attn
