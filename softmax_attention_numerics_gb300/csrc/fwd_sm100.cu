@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int n_mine = n_t[t];
         const int r0_tile = m0 + t * kTile;
         float m_ref = -INFINITY;
-        float l = 0.f;      // sum of the exact probabilities (-> lse)
-        float lr = 0.f;     // sum of the bf16-rounded probabilities fed to P V (-> out)
+        float2 l2 = make_float2(0.f, 0.f);    // sum of the exact probabilities (-> lse)
+        float2 lr2 = make_float2(0.f, 0.f);   // sum of the bf16-rounded ones fed to P V (-> out)
         bool ok = true;
 
         for (int j = 0; j < n_mine; ++j) {
@@ -285,13 +285,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     mt = fmaxf(mt, x[c]);
                 }
             } else {
+                // full tile, no mask: the max of the raw scores, scaled once
+                // (x stays unscaled; P below folds the scale into one FMA)
                 tmem_ld128(tS, reinterpret_cast<uint32_t*>(x));
+                float mr = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < kTile; ++c) {
-                    x[c] *= p.scale_log2;
-                    mt = fmaxf(mt, x[c]);
+                for (int c = 0; c < kTile; ++c) mr = fmaxf(mr, x[c]);
+                if (p.scale_log2 > 0.f) {
+                    mt = mr * p.scale_log2;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kTile; ++c) mt = fmaxf(mt, x[c] * p.scale_log2);
                 }
             }
+            const bool raw = !has_mask && !pred;   // x holds unscaled scores
             // Online max: always m_new = max(m_ref, m_tile); lazy threshold 8.
             const float m_new = fmaxf(m_ref, mt);
             bool rescale;
@@ -305,24 +312,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             float corr = 1.f;
             if (rescale) {
                 corr = ex2(m_ref - m_new);          // m_ref = -inf -> 0
-                l *= corr;
-                lr *= corr;
+                l2 = fmul2(l2, make_float2(corr, corr));
+                lr2 = fmul2(lr2, make_float2(corr, corr));
                 // O holds data only after the first PV; a row whose m_ref was
                 // -inf has O = 0 there and needs no correction.
                 if (j == 0 || m_ref == -INFINITY) corr = 1.f;
                 m_ref = m_new;
             }
             const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
+            const float2 nms2 = make_float2(-ms, -ms);
+            const float2 c2 = raw ? make_float2(p.scale_log2, p.scale_log2) : make_float2(1.f, 1.f);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2(fminf(x[32 * c + 2 * e] - ms, kLazyTau));
-                    const float p1 = ex2(fminf(x[32 * c + 2 * e + 1] - ms, kLazyTau));
-                    l += p0 + p1;
-                    pk[e] = pack_bf16(p0, p1);
-                    lr += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
+                    // x - m_ref in one packed FMA (the scale folded in when x is raw)
+                    const float2 d2 = ffma2(make_float2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), c2, nms2);
+                    float2 p2;
+                    if (raw && (e % 5) == 3) {
+                        p2 = exp2_poly2(d2);        // ~1 pair in 5 on the FMA pipe
+                    } else {
+                        p2.x = ex2(fminf(d2.x, kLazyTau));
+                        p2.y = ex2(fminf(d2.y, kLazyTau));
+                    }
+                    l2 = fadd2(l2, p2);
+                    pk[e] = pack_bf16(p2.x, p2.y);
+                    lr2 = fadd2(lr2, make_float2(__uint_as_float(pk[e] << 16),
+                                                 __uint_as_float(pk[e] & 0xffff0000u)));
                 }
                 tmem_st16(tS + 16 * c, pk);
             }
@@ -355,6 +372,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (ok) {
             // Normalise by the rounded sum: out stays an exact weighted mean of V
             // even when the lazy reference max lags (largest weight up to 2^8).
+            const float l = l2.x + l2.y, lr = lr2.x + lr2.y;
             const float inv = lr > 0.f ? 1.0f / lr : 0.f;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
