@@ -330,12 +330,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     // x - m_ref in one packed FMA (the scale folded in when x is raw)
                     const float2 d2 = ffma2(make_float2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), c2, nms2);
                     float2 p2;
-                    if (raw && (e % 5) == 3) {
-                        p2 = exp2_poly2(d2);        // ~1 pair in 5 on the FMA pipe
-                    } else {
-                        p2.x = ex2(fminf(d2.x, kLazyTau));
-                        p2.y = ex2(fminf(d2.y, kLazyTau));
-                    }
+                    p2.x = ex2(fminf(d2.x, kLazyTau));
+                    p2.y = ex2(fminf(d2.y, kLazyTau));
                     l2 = fadd2(l2, p2);
                     pk[e] = pack_bf16(p2.x, p2.y);
                     lr2 = fadd2(lr2, make_float2(__uint_as_float(pk[e] << 16),

@@ -172,30 +172,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     return r;
 }
 
-// 2^x on the FMA pipe for a pair of arguments, to take load off the MUFU
-// unit: x = n + f with n = round(x) (the 1.5 * 2^23 rounding trick), 2^f by a
-// cubic fitted for minimum relative error on [-1/2, 1/2] (Remez exchange;
-// csrc/gen_exp2_poly.py, max relative error 7.5e-5, far below bf16's 2^-9),
-// and 2^n added into the exponent field.  Arguments are clamped to
-// [-125, 8]: below -125 the result is 2^-125 instead of 0, so callers use it
-// only where no key is masked.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    constexpr float kRound = 12582912.0f;      // 1.5 * 2^23
-    x.x = fmaxf(fminf(x.x, 8.f), -125.f);
-    x.y = fmaxf(fminf(x.y, 8.f), -125.f);
-    const float2 t = fadd2(x, make_float2(kRound, kRound));
-    const float2 nr = fadd2(t, make_float2(-kRound, -kRound));
-    const float2 f = ffma2(nr, make_float2(-1.f, -1.f), x);
-    float2 q = ffma2(make_float2(5.517166853e-02f, 5.517166853e-02f), f,
-                     make_float2(2.426111251e-01f, 2.426111251e-01f));
-    q = ffma2(q, f, make_float2(6.932609677e-01f, 6.932609677e-01f));
-    q = ffma2(q, f, make_float2(9.999280572e-01f, 9.999280572e-01f));
-    // t's bit pattern is 0x4B400000 + n; shifted left by 23 the constant part
-    // vanishes modulo 2^32, leaving n in the exponent field.
-    return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
-                       __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
-}
-
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
