@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--seqlen", type=int, default=131072)
     ap.add_argument("--heads", type=int, default=16)
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="dQ by the per-query-tile kernel instead of fp32 reductions")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-oracle-reps", type=int, default=1, help=argparse.SUPPRESS)
@@ -56,8 +58,9 @@ def fwd_flops(B, H, S, D, causal):
 
 
 def workload_name(a):
-    return "long_seq B=1 H=%d S=%d D=128 %s fwd+bwd" % (
-        a.heads, a.seqlen, "causal" if a.causal else "non-causal")
+    return "long_seq B=1 H=%d S=%d D=128 %s fwd+bwd%s" % (
+        a.heads, a.seqlen, "causal" if a.causal else "non-causal",
+        " (deterministic dQ)" if a.deterministic else "")
 
 
 # ---------------------------------------------------------------- CPU oracle sample
@@ -287,7 +290,7 @@ def main():
     def step(s):
         attn_fwd(q, k, v, causal=a.causal, scale=scale, out=out, lse=lse, stream=s)
         attn_bwd(q, k, v, out, do, lse, causal=a.causal, scale=scale, dq=dq, dk=dk, dv=dv,
-                 workspace=ws, stream=s)
+                 workspace=ws, stream=s, deterministic=a.deterministic)
 
     stages = (_lib.ATTN_STAGE_FWD, _lib.ATTN_STAGE_BWD_PREPROCESS, _lib.ATTN_STAGE_BWD_MAIN,
               _lib.ATTN_STAGE_BWD_DQ)
@@ -340,7 +343,8 @@ def main():
 
     peaks, peak_kind = measured_peaks()
     tensor_peak = peaks.get("bf16_tflops_sustained", 1700.0)
-    main_flops = 2.5 * ff
+    # main kernel: S, dP, dV, dK (+ dQ unless the per-query-tile kernel does it)
+    main_flops = (2.0 if a.deterministic else 2.5) * ff
     main_achieved = main_flops / (stage_ms[_lib.ATTN_STAGE_BWD_MAIN] / 1e3) / 1e12
     traffic = ncu_traffic("bwd_main")
     roofline = {"bound": "tensor", "kernel": "bwd_main", "achieved": main_achieved,
@@ -356,7 +360,9 @@ def main():
         "bwd_main_ms": stage_ms[_lib.ATTN_STAGE_BWD_MAIN],
         "fwd_ms": stage_ms[_lib.ATTN_STAGE_FWD],
         "bwd_preprocess_gbs": pre_bytes / (stage_ms[_lib.ATTN_STAGE_BWD_PREPROCESS] / 1e3) / 1e9,
-        "dq_convert_gbs": dq_bytes / (stage_ms[_lib.ATTN_STAGE_BWD_DQ] / 1e3) / 1e9,
+        "bwd_dq_ms": stage_ms[_lib.ATTN_STAGE_BWD_DQ],
+        "dq_convert_gbs": (None if a.deterministic else
+                           dq_bytes / (stage_ms[_lib.ATTN_STAGE_BWD_DQ] / 1e3) / 1e9),
         "hbm_peak_gbs": peaks.get("hbm_gbs"),
         "nonfinite_outputs": nonfinite,
     }
@@ -374,7 +380,7 @@ def main():
         qq, kk, vv, dd = dq_in
         o, l = attn_fwd(qq, kk, vv, causal=a.causal, scale=scale, out=out, lse=lse, stream=s)
         attn_bwd(qq, kk, vv, o, dd, l, causal=a.causal, scale=scale, dq=dq, dk=dk, dv=dv,
-                 workspace=ws, stream=s)
+                 workspace=ws, stream=s, deterministic=a.deterministic)
         for hdst, dsrc in zip(host_out, (out, lse, dq, dk, dv)):
             hdst.copy_(dsrc, non_blocking=True)
 

@@ -13,14 +13,18 @@
 //            section 3).  Hidden entries are 0 by selection.
 //     dS^T = P^T o (dP^T - Delta)
 //     dV  += P^T dO_i, dK += dS^T Q_i       (TMEM accumulators, no atomics)
-//     dQ_i = dS K  -> fp32 vector reductions into the dQ workspace
-// Warps: 0-3 compute P^T / dS^T (thread = key row = TMEM lane); 4-7 read dQ_i
-// out of TMEM (thread = query row) and reduce it into global memory while the
-// next tile's MMAs run; 8 = TMA producer (+ lse2 / Delta vectors); 9 = TMEM
-// allocator and UMMA issuer.
-// TMEM: dV | dK (D columns each) | S^T | dP^T (128 each).  P^T (bf16) is
-// written over the first half of S^T and dS^T over the first half of dP^T;
-// dQ_i lands in the second halves (columns 64-127 of S^T, then of dP^T).
+//     dQ_i = dS K  -> fp32 bulk tensor reductions into the dQ workspace
+// Warps: 0-7 compute (thread = key row = TMEM lane; warps 0-3 take the
+// 32-query chunks 0 and 1, warps 4-7 chunks 2 and 3, two chunks at once), then
+// read their half of dQ_i out of TMEM (thread = query row) and stage it in
+// shared memory; 8 = TMA producer (+ lse2 / Delta vectors); 9 = TMEM allocator
+// and UMMA issuer; 10 = issues the dQ reductions and waits for them to read
+// the staging, so no compute warp ever blocks on the L2.
+// TMEM: dV | dK (D columns each) | S^T | dP^T (128 each).  Chunk c of S^T
+// (columns 32c .. 32c+31) is overwritten by its own packed bf16 P^T (first 16
+// columns) and dS^T (last 16) once read, so chunks never wait on each other;
+// dQ_i = dS K then takes dP^T's columns as one N = D accumulator.
+// dV / dK MMAs for chunks 0 and 2 run while chunks 1 and 3 are computed.
 //
 // Epilogue (PFCCLab/cudnn-frontend PR #9, section 1): every thread writes its
 // dK / dV row into a shared staging tile, fences its own writes for the async
@@ -36,8 +40,9 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 352;
 constexpr int kT = 128;
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpReduce = 10;
 
 template <int D>
 struct BwdLayout {
@@ -51,12 +56,13 @@ struct BwdLayout {
     static constexpr int kVec = kDS + kT * kT * 2;      // lse2[2][128], delta[2][128]
     static constexpr int kBar = kVec + 4 * kT * 4;
     static constexpr int kBarKV = 0;
-    static constexpr int kBarQFull = 1;                 // [2]
-    static constexpr int kBarQEmpty = 3;                // [2]
-    static constexpr int kBarSdp = 5;      // [2]: S^T and dP^T of query half 0 / 1 done
-    static constexpr int kBarP = 7;        // [2]: P^T, dS^T of query half 0 / 1 written
-    static constexpr int kBarDQFull = 9;
-    static constexpr int kBarDQRead = 10;
+    static constexpr int kBarQFull = 1;    // [2]
+    static constexpr int kBarQEmpty = 3;   // [2]: dV/dK MMAs done + dQ reduction read the stage
+    static constexpr int kBarSdp = 5;      // S^T and dP^T done
+    static constexpr int kBarP = 6;        // [2]: P^T, dS^T of chunks {0, 2} / {1, 3} written
+    static constexpr int kBarDQFull = 8;
+    static constexpr int kBarDQRead = 9;   // both dQ halves read out of TMEM
+    static constexpr int kBarDQStaged = 10;
     static constexpr int kBarAcc = 11;
     static constexpr int kBarDrain = 12;
     static constexpr int kNumBars = 13;
@@ -115,16 +121,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
         for (int i = 0; i < L::kNumBars; ++i) {
             uint32_t cnt = 1;
             if (i == L::kBarQFull || i == L::kBarQFull + 1) cnt = 33;
-            // q_empty: the MMAs' commit + the dQ warps once their reduction read the stage
+            // q_empty: the MMAs' commit + the reduction issuer once the stage was read
             if (i == L::kBarQEmpty || i == L::kBarQEmpty + 1) cnt = 2;
-            if (i == L::kBarP || i == L::kBarP + 1 || i == L::kBarDQRead) cnt = kT;
+            if (i == L::kBarP || i == L::kBarP + 1) cnt = 256;
+            if (i == L::kBarDQRead || i == L::kBarDQStaged) cnt = 256;
             mbar_init(bar(i), cnt);
         }
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
         tmem_relinquish();
     }
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
     // at the same time then reduce into different dQ rows instead of all
     // hammering the same L2 lines.
     const int rot = n_iter > 0 ? static_cast<int>(blockIdx.x % n_iter) : 0;
-    // Byte offset of fp32 dQ staging block `blk` inside query/dO stage `s`.
+    // Byte offset of fp32 dQ staging block `blk` (32 columns) inside query/dO stage `s`.
     auto dq_stage_off = [&](int blk, int s) {
         return ((blk & 1) ? L::kDO : L::kQ) + s * L::kTileBytes + (blk >> 1) * 16384;
     };
@@ -149,7 +156,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
         *h = hk * p.G + gi;
     };
 
-    if (warp == 8) {
+    if (warp == kWarpProducer) {
         // ------------------------------------------------------------ producer (whole warp)
         bool ok = true;
         if (lane == 0) {
@@ -203,12 +210,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 mbar_wait(bar(L::kBarQFull + (it & 1)), (it >> 1) & 1, &no_abort);
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ UMMA issuer
         if (lane == 0) {
-            constexpr uint32_t id_half = idesc_bf16(128, 64, 0, 0);    // S^T, dP^T halves
+            constexpr uint32_t id_sdp = idesc_bf16(128, 128, 0, 0);    // S^T, dP^T
             constexpr uint32_t id_acc = idesc_bf16(128, D, 0, 1);      // dV, dK (B MN-major)
-            constexpr uint32_t id_dq = idesc_bf16(128, 64, 1, 1);      // dQ halves
+            constexpr uint32_t id_dq = idesc_bf16(128, D, 1, 1);       // dQ (A, B MN-major)
             const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP;
             const uint32_t tDV = tmem + L::kColDV, tDK = tmem + L::kColDK;
             const uint64_t k_k = smem_desc(sbase + L::kK, 16, 1024, kSwizzle128B);
@@ -229,49 +236,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 const uint64_t do_k = smem_desc(da, 16, 1024, kSwizzle128B);
                 const uint64_t q_mn = smem_desc(qa, 16384, 1024, kSwizzle128B);  // MN-major
                 const uint64_t do_mn = smem_desc(da, 16384, 1024, kSwizzle128B);
-                // S^T and dP^T in two query halves (N = 64) so that the compute
-                // warps start on half 0 while the tensor core produces half 1.
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tS + 64 * hf, desc_add(k_k, off), desc_add(q_k, off + 8192 * hf),
-                               id_half, kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tDP + 64 * hf, desc_add(v_k, off), desc_add(do_k, off + 8192 * hf),
-                               id_half, kk > 0);
-                    }
-                    mma_commit(bar(L::kBarSdp + hf));
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tS, desc_add(k_k, off), desc_add(q_k, off), id_sdp, kk > 0);
                 }
-                // dV += P^T dO, dK += dS^T Q, one query half at a time as P^T and
-                // dS^T of that half arrive.
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    if (!(ok = mbar_wait(bar(L::kBarP + hf), it & 1, abort_flag))) break;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tDP, desc_add(v_k, off), desc_add(do_k, off), id_sdp, kk > 0);
+                }
+                mma_commit(bar(L::kBarSdp));
+                // dV += P^T dO, dK += dS^T Q as the chunks arrive: phase 0 covers
+                // chunks 0 and 2, phase 1 chunks 1 and 3 (16 queries = 8 packed
+                // columns per step; P^T at 32c, dS^T at 32c + 16).
+#pragma unroll
+                for (int ph = 0; ph < 2; ++ph) {
+                    if (!(ok = mbar_wait(bar(L::kBarP + ph), it & 1, abort_flag))) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int kq = 0; kq < 4; ++kq) {
-                        const int kk = 4 * hf + kq;
-                        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                        mma_ts(tDV, tS + kk * 8, desc_add(do_mn, kk * 2048), id_acc, acc);
-                        mma_ts(tDK, tDP + kk * 8, desc_add(q_mn, kk * 2048), id_acc, acc);
+                    for (int cq = 0; cq < 2; ++cq) {
+                        const int c = ph + 2 * cq;
+#pragma unroll
+                        for (int kq = 0; kq < 2; ++kq) {
+                            const int kk = 2 * c + kq;
+                            const uint32_t acc = (it > 0 || ph > 0 || cq > 0 || kq > 0) ? 1u : 0u;
+                            mma_ts(tDV, tS + 32 * c + 8 * kq, desc_add(do_mn, kk * 2048), id_acc, acc);
+                            mma_ts(tDK, tS + 32 * c + 16 + 8 * kq, desc_add(q_mn, kk * 2048), id_acc, acc);
+                        }
                     }
                 }
                 if (!ok) break;
                 mma_commit(bar(L::kBarQEmpty + s));
                 if (with_dq) {
+                    // dP^T's columns are free: every compute warp has read them.
 #pragma unroll
-                    for (int hh = 0; hh < L::kBlocks; ++hh) {
-                        const uint32_t dst = (hh == 0 ? tS : tDP) + 64;
-#pragma unroll
-                        for (int kk = 0; kk < kT / 16; ++kk)
-                            mma_ss(dst, desc_add(ds_mn, kk * 2048),
-                                   desc_add(k_mn, hh * 16384 + kk * 2048), id_dq, kk > 0);
-                    }
+                    for (int kk = 0; kk < kT / 16; ++kk)
+                        mma_ss(tDP, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), id_dq, kk > 0);
                 }
                 mma_commit(bar(L::kBarDQFull));
             }
@@ -283,11 +284,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ P^T / dS^T
-        const int r = warp * 32 + lane;             // key row in the tile = TMEM lane
+    } else if (warp == kWarpReduce) {
+        // ------------------------------------------------------------ dQ reduction issuer
+        // Reduce each staged dQ_i into the fp32 workspace with bulk tensor
+        // reductions; the stage returns to the producer once they have read it.
+        if (lane == 0) {
+            bool ok = true;
+            for (int it = 0; ok && it < n_iter; ++it) {
+                const int s = it & 1;
+                if (!(ok = mbar_wait(bar(L::kBarDQStaged), it & 1, abort_flag))) break;
+                if (with_dq) {
+                    int h, m0;
+                    iter_tile(it, &h, &m0);
+                    const int acc_row = static_cast<int>(b * p.acc_b) + row_base + m0;
+#pragma unroll
+                    for (int blk = 0; blk < D / 32; ++blk)
+                        tma_reduce_add_3d(&maps.dq_acc, sbase + dq_stage_off(blk, s), 32 * blk, h,
+                                          acc_row);
+                    bulk_commit();
+                    bulk_wait_read_all();          // only the committing thread may wait
+                }
+                mbar_arrive(bar(L::kBarQEmpty + s));
+            }
+        }
+        __syncwarp();
+        named_bar_sync(3, 160);    // warps 4-7 may reuse query stage 0 for the dK epilogue
+    } else {
+        // ------------------------------------------------------------ compute (warps 0-7)
+        const int wq = warp & 3;                    // TMEM lane quarter
+        const int hq = warp >> 2;                   // query half (P^T / dS^T), d half (dQ)
+        const int r = wq * 32 + lane;               // key row = TMEM lane (dQ: query row)
         const int j = n0 + r;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + L::kColS;
         const uint32_t tDP = tmem + lane_off + L::kColDP;
         uint8_t* ds_tile = smem + L::kDS;
@@ -299,242 +327,171 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             const float* lse2 = vec + s * 256;
             const bool pred = (n0 + kT > si.len_k) || (m0 + kT > si.len_q) ||
                               (p.causal && n0 + kT - 1 > m0) || (p.mask_kind != MASK_NONE);
-            // Query half hf (columns 64 hf .. 64 hf + 63) as soon as its S^T, dP^T land.
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-            // q_full[s] also publishes the producer's lse2 / Delta vectors.
-            ok = (hf > 0 || mbar_wait(bar(L::kBarQFull + s), (it >> 1) & 1, abort_flag)) &&
-                 mbar_wait(bar(L::kBarSdp + hf), it & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
+            // After a wait gives up, `ok` stays false: the warp skips the work
+            // but still meets every named barrier, so none is left short.
+            if (ok) {
+                // q_full[s] also publishes the producer's lse2 / Delta vectors.
+                ok = mbar_wait(bar(L::kBarQFull + s), (it >> 1) & 1, abort_flag) &&
+                     mbar_wait(bar(L::kBarSdp), it & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
             }
-            tc_fence_after();
-            if (p.mask_kind != MASK_NONE) {
-                // With a user mask, rewrite this half of S^T in TMEM as finished
-                // logits first (mask loads in the main loop would spill registers).
+            if (ok) {
+                tc_fence_after();
+                if (p.mask_kind != MASK_NONE) {
+                    // With a user mask, rewrite this warp's chunks of S^T in TMEM as
+                    // finished logits first (mask loads in the main loop would spill).
+#pragma unroll 1
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * hq + cc;
+                        uint32_t v[32];
+                        tmem_ld32(tS + 32 * c, v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = __float_as_uint(logit_log2(p, __uint_as_float(v[e]), b, h,
+                                                              m0 + 32 * c + e, j, si.len_q, si.len_k));
+                        tmem_st32(tS + 32 * c, v);
+                    }
+                    tmem_wait_st();
+                }
 #pragma unroll 1
                 for (int cc = 0; cc < 2; ++cc) {
-                    const int c = 2 * hf + cc;
-                    uint32_t v[32];
-                    tmem_ld32(tS + 32 * c, v);
+                    const int c = 2 * hq + cc;
+                    uint32_t sv[32], dv[32];
+                    tmem_ld32x2(tS + 32 * c, sv, tDP + 32 * c, dv);
+                    // -lse2 / Delta of this chunk's query rows, four at a time right
+                    // before use (16-byte shared loads, every lane the same address):
+                    // loading all 32 up front costs 64 live registers.
+                    const uint32_t va = smem_u32(lse2 + 32 * c);
+                    uint32_t pk[16], dk[16];
+                    if (!pred && p.mask_kind == MASK_NONE) {
+                        const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+                        float4 lv, dl;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = __float_as_uint(logit_log2(p, __uint_as_float(v[e]), b, h,
-                                                          m0 + 32 * c + e, j, si.len_q, si.len_k));
-                    tmem_st32(tS + 32 * c, v);
-                }
-                tmem_wait_st();
-            }
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * hf + cc;
-                uint32_t sv[32], dv[32];
-                tmem_ld32x2(tS + 32 * c, sv, tDP + 32 * c, dv);
-                // -lse2 / Delta of this chunk's 32 query rows: 16 independent
-                // 16-byte shared loads (every lane reads the same address).
-                float lv[32], dl[32];
-                const uint32_t va = smem_u32(lse2 + 32 * c);
-#pragma unroll
-                for (int v4 = 0; v4 < 8; ++v4) {
-                    const float4 a = lds128(va + 16 * v4);
-                    const float4 d = lds128(va + 512 + 16 * v4);
-                    lv[4 * v4] = a.x; lv[4 * v4 + 1] = a.y; lv[4 * v4 + 2] = a.z; lv[4 * v4 + 3] = a.w;
-                    dl[4 * v4] = d.x; dl[4 * v4 + 1] = d.y; dl[4 * v4 + 2] = d.z; dl[4 * v4 + 3] = d.w;
-                }
-                uint32_t pk[16], dk[16];
-                if (!pred && p.mask_kind == MASK_NONE) {
-                    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        // packed pairs: x - lse2 = s*c + (-lse2); dP - Delta; P*(dP - Delta)
-                        const float2 x2 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                                c2, make_float2(lv[e], lv[e + 1]));
-                        const float p0 = ex2(fminf(x2.x, 0.f));
-                        const float p1 = ex2(fminf(x2.y, 0.f));
-                        const float2 d2 = fadd2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
-                                                make_float2(-dl[e], -dl[e + 1]));
-                        const float2 ds2 = fmul2(make_float2(p0, p1), d2);
-                        pk[e >> 1] = pack_bf16(p0, p1);
-                        dk[e >> 1] = pack_bf16(ds2.x, ds2.y);
-                    }
-                } else if (p.mask_kind == MASK_NONE) {
-                    // keys past the sequence, query rows past it, causal pairs
-                    const int qlo = p.causal ? j - m0 : -1;          // visible: q >= qlo
-                    const int qhi = (j < si.len_k) ? si.len_q - m0 : 0;  // visible: q < qhi
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float pr[2], ds[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int q = 32 * c + e + u;
-                            const bool vis = q >= qlo && q < qhi;
-                            const float x = __uint_as_float(sv[e + u]) * p.scale_log2;
-                            const float pv = ex2(fminf(x + lv[e + u], 0.f));
-                            pr[u] = vis ? pv : 0.f;
-                            ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dl[e + u]) : 0.f;
+                        for (int e = 0; e < 32; e += 2) {
+                            if ((e & 3) == 0) {
+                                lv = lds128(va + 4 * e);
+                                dl = lds128(va + 512 + 4 * e);
+                            }
+                            const float2 l2 = (e & 2) ? make_float2(lv.z, lv.w) : make_float2(lv.x, lv.y);
+                            const float2 nd2 = (e & 2) ? make_float2(-dl.z, -dl.w) : make_float2(-dl.x, -dl.y);
+                            // packed pairs: x - lse2 = s*c + (-lse2); dP - Delta; P*(dP - Delta)
+                            const float2 x2 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                    c2, l2);
+                            const float p0 = ex2(fminf(x2.x, 0.f));
+                            const float p1 = ex2(fminf(x2.y, 0.f));
+                            const float2 d2 = fadd2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                                    nd2);
+                            const float2 ds2 = fmul2(make_float2(p0, p1), d2);
+                            pk[e >> 1] = pack_bf16(p0, p1);
+                            dk[e >> 1] = pack_bf16(ds2.x, ds2.y);
                         }
-                        pk[e >> 1] = pack_bf16(pr[0], pr[1]);
-                        dk[e >> 1] = pack_bf16(ds[0], ds[1]);
-                    }
-                } else {
-                    // mask: S^T already holds the finished log2-domain logits
+                    } else if (p.mask_kind == MASK_NONE) {
+                        // keys past the sequence, query rows past it, causal pairs
+                        const int qlo = p.causal ? j - m0 : -1;          // visible: q >= qlo
+                        const int qhi = (j < si.len_k) ? si.len_q - m0 : 0;  // visible: q < qhi
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float pr[2], ds[2];
+                        for (int e = 0; e < 32; e += 2) {
+                            float pr[2], ds[2];
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const float x = __uint_as_float(sv[e + u]);
-                            const bool vis = x != -INFINITY;
-                            const float pv = ex2(fminf(x + lv[e + u], 0.f));
-                            pr[u] = vis ? pv : 0.f;
-                            ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dl[e + u]) : 0.f;
+                            for (int u = 0; u < 2; ++u) {
+                                const int q = 32 * c + e + u;
+                                const bool vis = q >= qlo && q < qhi;
+                                const float x = __uint_as_float(sv[e + u]) * p.scale_log2;
+                                const float nl = lds32(va + 4 * (e + u)), dt = lds32(va + 512 + 4 * (e + u));
+                                const float pv = ex2(fminf(x + nl, 0.f));
+                                pr[u] = vis ? pv : 0.f;
+                                ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dt) : 0.f;
+                            }
+                            pk[e >> 1] = pack_bf16(pr[0], pr[1]);
+                            dk[e >> 1] = pack_bf16(ds[0], ds[1]);
                         }
-                        pk[e >> 1] = pack_bf16(pr[0], pr[1]);
-                        dk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                    } else {
+                        // mask: S^T already holds the finished log2-domain logits
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float pr[2], ds[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const float x = __uint_as_float(sv[e + u]);
+                                const bool vis = x != -INFINITY;
+                                const float nl = lds32(va + 4 * (e + u)), dt = lds32(va + 512 + 4 * (e + u));
+                                const float pv = ex2(fminf(x + nl, 0.f));
+                                pr[u] = vis ? pv : 0.f;
+                                ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dt) : 0.f;
+                            }
+                            pk[e >> 1] = pack_bf16(pr[0], pr[1]);
+                            dk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                        }
                     }
-                }
-                tmem_st16(tS + 16 * c, pk);
-                tmem_st16(tDP + 16 * c, dk);
-                if (with_dq) stage_row_chunk(ds_tile, r, 32 * c, dk);
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();      // dS in shared memory -> the dQ MMA
-            tc_fence_before();
-            mbar_arrive(bar(L::kBarP + hf));
-            }
-            if (!ok) break;
-        }
-        // dV epilogue: staging tile = the dS buffer (free once every MMA is done).
-        if (ok) {
-            ok = mbar_wait(bar(L::kBarAcc), 0, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        {
-            if (ok) tc_fence_after();
-            const bool tma_path = !p.varlen || n0 + kT <= si.len_k;
-            bf16* grow = p.dv + b * p.dk_b + static_cast<int64_t>(row_base + j) * p.dk_s + hk * p.dk_h;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                if (ok && n_iter > 0) {
-                    tmem_ld32(tmem + lane_off + L::kColDV + 32 * c, o);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
-                if (!ok) {
-                } else if (tma_path) {
-                    stage_row_chunk(ds_tile, r, 32 * c, pk);
-                } else if (j < si.len_k) {
-                    uint4* dst = reinterpret_cast<uint4*>(grow + 32 * c);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    tmem_st16(tS + 32 * c, pk);
+                    tmem_st16(tS + 32 * c + 16, dk);
+                    if (with_dq) stage_row_chunk(ds_tile, r, 32 * c, dk);
+                    tmem_wait_st();
+                    fence_proxy_async_smem();      // dS in shared memory -> the dQ MMA
+                    tc_fence_before();
+                    mbar_arrive(bar(L::kBarP + cc));
                 }
             }
-            if (tma_path) {
-                if (ok) fence_proxy_async_smem();   // each writer: its stores -> async proxy
-                named_bar_sync(1, 128);             // all 128 rows are in the staging tile
-                if (ok && r == 0) {
-#pragma unroll
-                    for (int c = 0; c < L::kBlocks; ++c)
-                        tma_store_4d(&maps.dv, sbase + L::kDS + c * 16384, 64 * c, hk, row_base + n0,
-                                     bcoord);
-                    bulk_commit();
-                    bulk_wait_read_all();   // only the committing thread may wait
-                }
-                named_bar_sync(1, 128);     // staging tile no longer read
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ dQ read-out (warps 4-7)
-        const int wq = warp & 3;
-        const int r = wq * 32 + lane;               // query row in the tile = TMEM lane
-        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        bool ok = true;
-        for (int it = 0; it < n_iter; ++it) {
-            int h, m0;
-            iter_tile(it, &h, &m0);
-            // After a wait gives up, `ok` stays false: the warp skips the work but
-            // still meets every named barrier, so none is left short.
+            // dQ_i: this warp's D/2 columns for its 32 query rows, out of TMEM,
+            // then staged as fp32 in this tile's query/dO stage (every MMA that
+            // read the stage has completed once dq_full fires).
             if (ok) {
                 ok = mbar_wait(bar(L::kBarDQFull), it & 1, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
             }
-            float dq[D];
             if (ok) {
                 tc_fence_after();
+                uint32_t dq[D / 2];
                 if (with_dq) {
-#pragma unroll
-                    for (int hh = 0; hh < L::kBlocks; ++hh) {
-                        const uint32_t src = tmem + lane_off + (hh == 0 ? L::kColS : L::kColDP) + 64;
-                        tmem_ld32x2(src, reinterpret_cast<uint32_t*>(dq) + 64 * hh, src + 32,
-                                    reinterpret_cast<uint32_t*>(dq) + 64 * hh + 32);
+                    const uint32_t src = tDP + hq * (D / 2);
+                    if constexpr (D == 128) {
+                        tmem_ld32x2(src, dq, src + 32, dq + 32);
+                    } else {
+                        tmem_ld32(src, dq);
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(bar(L::kBarDQRead));
-            }
-            // Reduce dQ_i into the fp32 workspace with bulk tensor reductions,
-            // staged in this tile's query/dO stage: every MMA that read it has
-            // completed (dq_full covers them), and the stage returns to the
-            // producer only once the reductions have read the staging.
-            const int s = it & 1;
-            if (with_dq) {
-                if (ok) {
-                    // fp32 staging: D/32 blocks of [128 rows][128 B], 16-byte chunks
-                    // swizzled; even blocks in the query stage, odd ones in the dO stage.
 #pragma unroll
-                    for (int blk = 0; blk < D / 32; ++blk) {
-                        uint8_t* base = smem + dq_stage_off(blk, s);
+                for (int bb = 0; bb < D / 64; ++bb) {
+                    if (with_dq) {
+                        // fp32 staging: 32-column blocks of [128 rows][128 B], 16-byte
+                        // chunks swizzled; even blocks in the query stage, odd in the dO stage.
+                        uint8_t* base = smem + dq_stage_off(hq * (D / 64) + bb, s) + r * 128;
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            float4* dst = reinterpret_cast<float4*>(base + r * 128 + ((k ^ (r & 7)) << 4));
-                            *dst = make_float4(dq[32 * blk + 4 * k], dq[32 * blk + 4 * k + 1],
-                                               dq[32 * blk + 4 * k + 2], dq[32 * blk + 4 * k + 3]);
-                        }
+                        for (int k = 0; k < 8; ++k)
+                            *reinterpret_cast<uint4*>(base + ((k ^ (r & 7)) << 4)) =
+                                make_uint4(dq[32 * bb + 4 * k], dq[32 * bb + 4 * k + 1],
+                                           dq[32 * bb + 4 * k + 2], dq[32 * bb + 4 * k + 3]);
                     }
-                    fence_proxy_async_smem();      // each writer: its stores -> async proxy
                 }
-                named_bar_sync(2, 128);            // the whole 128 x D tile is staged
-                if (ok && r == 0) {
-                    const int acc_row = static_cast<int>(b * p.acc_b) + row_base + m0;
-#pragma unroll
-                    for (int blk = 0; blk < D / 32; ++blk)
-                        tma_reduce_add_3d(&maps.dq_acc, sbase + dq_stage_off(blk, s), 32 * blk, h,
-                                          acc_row);
-                    bulk_commit();
-                    bulk_wait_read_all();          // only the committing thread may wait
-                    mbar_arrive(bar(L::kBarQEmpty + s));
-                }
-            } else if (ok && r == 0) {
-                mbar_arrive(bar(L::kBarQEmpty + s));
+                if (with_dq) fence_proxy_async_smem();   // each writer: its stores -> async proxy
+                mbar_arrive(bar(L::kBarDQStaged));
             }
         }
-        // dK epilogue: staging tile = query stage 0 (free once every MMA is done
-        // and the last dQ reduction has read it: its issuer waited for that
-        // before this barrier).
-        named_bar_sync(2, 128);
+        // Epilogue: warps 0-3 store dV (staging tile = the dS buffer), warps 4-7
+        // dK (staging tile = query stage 0, free once the reduction issuer has
+        // seen its last reduction read it).  Both need every MMA done.
+        const int nb = hq ? 2 : 1;                   // named barrier of this warpgroup
+        if (hq) named_bar_sync(3, 160);
         if (ok) {
             ok = mbar_wait(bar(L::kBarAcc), 0, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
         {
             if (ok) tc_fence_after();
-            const int j = n0 + r;
-            uint8_t* tile = smem + L::kQ;
+            uint8_t* tile = hq ? smem + L::kQ : ds_tile;
+            const uint32_t tile_addr = sbase + (hq ? L::kQ : L::kDS);
+            const uint32_t col = hq ? L::kColDK : L::kColDV;
+            const float mul = hq ? p.scale : 1.f;    // dK = scale * dS^T Q
             const bool tma_path = !p.varlen || n0 + kT <= si.len_k;
-            bf16* grow = p.dk + b * p.dk_b + static_cast<int64_t>(row_base + j) * p.dk_s + hk * p.dk_h;
+            bf16* grow = (hq ? p.dk : p.dv) + b * p.dk_b + static_cast<int64_t>(row_base + j) * p.dk_s +
+                         hk * p.dk_h;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
                 if (ok && n_iter > 0) {
-                    tmem_ld32(tmem + lane_off + L::kColDK + 32 * c, o);
+                    tmem_ld32(tmem + lane_off + col + 32 * c, o);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
@@ -542,8 +499,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * p.scale,
-                                      __uint_as_float(o[2 * e + 1]) * p.scale);
+                    pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * mul,
+                                      __uint_as_float(o[2 * e + 1]) * mul);
                 if (!ok) {
                 } else if (tma_path) {
                     stage_row_chunk(tile, r, 32 * c, pk);
@@ -555,24 +512,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 }
             }
             if (tma_path) {
-                if (ok) fence_proxy_async_smem();
-                named_bar_sync(2, 128);
+                if (ok) fence_proxy_async_smem();   // each writer: its stores -> async proxy
+                named_bar_sync(nb, 128);            // all 128 rows are in the staging tile
                 if (ok && r == 0) {
 #pragma unroll
                     for (int c = 0; c < L::kBlocks; ++c)
-                        tma_store_4d(&maps.dk, sbase + L::kQ + c * 16384, 64 * c, hk, row_base + n0,
-                                     bcoord);
+                        tma_store_4d(hq ? &maps.dk : &maps.dv, tile_addr + c * 16384, 64 * c, hk,
+                                     row_base + n0, bcoord);
                     bulk_commit();
-                    bulk_wait_read_all();
+                    bulk_wait_read_all();   // only the committing thread may wait
                 }
-                named_bar_sync(2, 128);
+                named_bar_sync(nb, 128);    // staging tile no longer read
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, L::kTmemCols);
     }

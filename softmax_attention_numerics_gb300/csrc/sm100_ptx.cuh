@@ -135,6 +135,12 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 }
 
 // 16-byte shared-memory load from a 32-bit shared address.
+__device__ __forceinline__ float lds32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ float4 lds128(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
