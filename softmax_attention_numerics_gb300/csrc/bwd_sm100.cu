@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
     auto bar = [&](int i) { return sbase + L::kBar + 8u * i; };
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
-    float* vec = reinterpret_cast<float*>(smem + L::kVec);   // lse2[s][128] at s*256, delta at +128
+    float* vec = reinterpret_cast<float*>(smem + L::kVec);   // -lse2[s][128] at s*256, -delta at +128
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, hk = blockIdx.y;
@@ -197,8 +197,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 const int i = m0 + q;
                 const int64_t li = b * p.lse_b + h * p.lse_h + row_base + i;
                 const bool in = i < si.len_q;
-                vec[s * 256 + q] = in ? -p.lse2[li] : 0.f;     // stored negated
-                vec[s * 256 + 128 + q] = in ? p.delta[li] : 0.f;
+                vec[s * 256 + q] = in ? -p.lse2[li] : 0.f;     // both stored negated
+                vec[s * 256 + 128 + q] = in ? -p.delta[li] : 0.f;
             }
             mbar_arrive(bar(L::kBarQFull + s));
             issued = it + 1;
@@ -358,22 +358,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                     const int c = 2 * hq + cc;
                     uint32_t sv[32], dv[32];
                     tmem_ld32x2(tS + 32 * c, sv, tDP + 32 * c, dv);
-                    // -lse2 / Delta of this chunk's query rows, four at a time right
-                    // before use (16-byte shared loads, every lane the same address):
-                    // loading all 32 up front costs 64 live registers.
+                    // -lse2 / -Delta of this chunk's query rows, four at a time, one
+                    // group ahead of use (16-byte shared loads, every lane the same
+                    // address): loading all 32 up front costs 64 live registers.
                     const uint32_t va = smem_u32(lse2 + 32 * c);
                     uint32_t pk[16], dk[16];
                     if (!pred && p.mask_kind == MASK_NONE) {
                         const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-                        float4 lv, dl;
+                        float4 lv = lds128(va), dl = lds128(va + 512), lvn, dln;
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            if ((e & 3) == 0) {
-                                lv = lds128(va + 4 * e);
-                                dl = lds128(va + 512 + 4 * e);
+                            if ((e & 3) == 0 && e + 4 < 32) {
+                                lvn = lds128(va + 4 * e + 16);
+                                dln = lds128(va + 512 + 4 * e + 16);
                             }
                             const float2 l2 = (e & 2) ? make_float2(lv.z, lv.w) : make_float2(lv.x, lv.y);
-                            const float2 nd2 = (e & 2) ? make_float2(-dl.z, -dl.w) : make_float2(-dl.x, -dl.y);
+                            const float2 nd2 = (e & 2) ? make_float2(dl.z, dl.w) : make_float2(dl.x, dl.y);
                             // packed pairs: x - lse2 = s*c + (-lse2); dP - Delta; P*(dP - Delta)
                             const float2 x2 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
                                                     c2, l2);
@@ -384,6 +384,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                             const float2 ds2 = fmul2(make_float2(p0, p1), d2);
                             pk[e >> 1] = pack_bf16(p0, p1);
                             dk[e >> 1] = pack_bf16(ds2.x, ds2.y);
+                            if ((e & 3) == 2) {
+                                lv = lvn;
+                                dl = dln;
+                            }
                         }
                     } else if (p.mask_kind == MASK_NONE) {
                         // keys past the sequence, query rows past it, causal pairs
@@ -397,10 +401,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                                 const int q = 32 * c + e + u;
                                 const bool vis = q >= qlo && q < qhi;
                                 const float x = __uint_as_float(sv[e + u]) * p.scale_log2;
-                                const float nl = lds32(va + 4 * (e + u)), dt = lds32(va + 512 + 4 * (e + u));
+                                const float nl = lds32(va + 4 * (e + u)), nd = lds32(va + 512 + 4 * (e + u));
                                 const float pv = ex2(fminf(x + nl, 0.f));
                                 pr[u] = vis ? pv : 0.f;
-                                ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dt) : 0.f;
+                                ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) + nd) : 0.f;
                             }
                             pk[e >> 1] = pack_bf16(pr[0], pr[1]);
                             dk[e >> 1] = pack_bf16(ds[0], ds[1]);
@@ -414,10 +418,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                             for (int u = 0; u < 2; ++u) {
                                 const float x = __uint_as_float(sv[e + u]);
                                 const bool vis = x != -INFINITY;
-                                const float nl = lds32(va + 4 * (e + u)), dt = lds32(va + 512 + 4 * (e + u));
+                                const float nl = lds32(va + 4 * (e + u)), nd = lds32(va + 512 + 4 * (e + u));
                                 const float pv = ex2(fminf(x + nl, 0.f));
                                 pr[u] = vis ? pv : 0.f;
-                                ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dt) : 0.f;
+                                ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) + nd) : 0.f;
                             }
                             pk[e >> 1] = pack_bf16(pr[0], pr[1]);
                             dk[e >> 1] = pack_bf16(ds[0], ds[1]);
