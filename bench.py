@@ -232,7 +232,7 @@ def run_reference(a):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": workload_name(a), "B": 1, "H": a.heads, "S": a.seqlen, "D": 128,
-                   "causal": a.causal, "parallelism": "replicas",
+                   "causal": a.causal, "parallelism": "replicas" if a.gpus > 1 else "single",
                    "sample": "each step: fp64 oracle on query rows 0..%d of one head" % (rows - 1)},
         "cpu_baseline": cb,
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
