@@ -35,7 +35,7 @@ KERNEL_SOURCES = ("softmax_attention_numerics_gb300/csrc/bwd_sm100.cu",
                   "softmax_attention_numerics_gb300/csrc/device_common.cuh")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-oracle-reps", type=int, default=1, help=argparse.SUPPRESS)
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def fwd_flops(B, H, S, D, causal):
@@ -190,6 +190,24 @@ def measured_peaks():
             "fallback"
 
 
+def max_over_ranks(x, device=None):
+    """The largest value of `x` over all ranks of the default process group
+    (the value itself when there is no group or one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(fwd_flop, steps, world, ms):
+    """Whole-job throughput: every rank ran `steps` fwd+bwd steps of `fwd_flop`
+    forward flop each (backward = 2.5x), in at most `ms` milliseconds."""
+    return 3.5 * fwd_flop * steps * world / (ms / 1e3) / 1e12
+
+
 def source_hash():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -326,11 +344,8 @@ def main():
         stream.synchronize()
     launches = lib.attn_launch_count() - launches0
     torch.cuda.synchronize(dev)
-    ms = t0.elapsed_time(t1)
+    ms = max_over_ranks(t0.elapsed_time(t1), dev)
     if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
         dist.barrier()
 
     # Non-finite check of the last step's results.
@@ -338,8 +353,7 @@ def main():
 
     stage_ms = {st: statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev[st]) for st in stages}
     ff = fwd_flops(B, H, S, D, a.causal)
-    total_flops = 3.5 * ff * a.steps * world
-    value = total_flops / (ms / 1e3) / 1e12
+    value = job_tflops(ff, a.steps, world, ms)
 
     peaks, peak_kind = measured_peaks()
     tensor_peak = peaks.get("bf16_tflops_sustained", 1700.0)
@@ -397,12 +411,8 @@ def main():
             e2e_step(stream)
         c1.record(stream)
     stream.synchronize()
-    e_ms = c0.elapsed_time(c1)
-    if world > 1:
-        tt = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e_ms = float(tt.item())
-    e2e_value = 3.5 * ff * e_steps * world / (e_ms / 1e3) / 1e12
+    e_ms = max_over_ranks(c0.elapsed_time(c1), dev)
+    e2e_value = job_tflops(ff, e_steps, world, e_ms)
 
     if rank == 0:
         line = {
