@@ -382,36 +382,77 @@ def main():
     }
 
     # End-to-end through the public API with host buffers (pinned), copies timed.
+    # Pipelined like an input pipeline would be: step i+1's inputs are copied in
+    # on one copy stream and step i's outputs copied out on another while the
+    # compute stream runs step i+1; inputs and outputs are double-buffered on
+    # the device.  The timed region runs from the first input copy to the end of
+    # the last output copy, so every step's copies are inside it.
     host_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out, lse, dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    dq_in = [torch.empty_like(t) for t in (q, k, v, do)]
+    dev_in = [[torch.empty_like(t) for t in (q, k, v, do)] for _ in range(2)]
+    dev_out = [[out, lse, dq, dk, dv], [torch.empty_like(t) for t in (out, lse, dq, dk, dv)]]
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    new_ev = lambda: torch.cuda.Event()
+    done_in = [new_ev() for _ in range(2)]      # inputs of buffer b are on the device
+    done_step = [new_ev() for _ in range(2)]    # compute on buffer b finished
+    done_out = [new_ev() for _ in range(2)]     # outputs of buffer b are on the host
 
-    def e2e_step(s):
-        for hdst, hsrc in zip(dq_in, host_in):
-            hdst.copy_(hsrc, non_blocking=True)
-        qq, kk, vv, dd = dq_in
-        o, l = attn_fwd(qq, kk, vv, causal=a.causal, scale=scale, out=out, lse=lse, stream=s)
-        attn_bwd(qq, kk, vv, o, dd, l, causal=a.causal, scale=scale, dq=dq, dk=dk, dv=dv,
-                 workspace=ws, stream=s, deterministic=a.deterministic)
-        for hdst, dsrc in zip(host_out, (out, lse, dq, dk, dv)):
-            hdst.copy_(dsrc, non_blocking=True)
+    def copy_in(i):
+        bb = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(done_step[bb])        # step i-2 no longer reads them
+            for hdst, hsrc in zip(dev_in[bb], host_in):
+                hdst.copy_(hsrc, non_blocking=True)
+            done_in[bb].record(s_in)
+
+    def compute(i):
+        bb = i % 2
+        with torch.cuda.stream(stream):
+            stream.wait_event(done_in[bb])
+            if i >= 2:
+                stream.wait_event(done_out[bb])       # step i-2's outputs left
+            qq, kk, vv, dd = dev_in[bb]
+            o_, l_, dq_, dk_, dv_ = dev_out[bb]
+            attn_fwd(qq, kk, vv, causal=a.causal, scale=scale, out=o_, lse=l_, stream=stream)
+            attn_bwd(qq, kk, vv, o_, dd, l_, causal=a.causal, scale=scale, dq=dq_, dk=dk_, dv=dv_,
+                     workspace=ws, stream=stream, deterministic=a.deterministic)
+            done_step[bb].record(stream)
+
+    def copy_out(i):
+        bb = i % 2
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done_step[bb])
+            for hdst, dsrc in zip(host_out, dev_out[bb]):
+                hdst.copy_(dsrc, non_blocking=True)
+            done_out[bb].record(s_out)
+
+    def run_pipeline(n, marks=None):
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            compute(i)
+            copy_out(i)
+            if marks is not None:
+                s_out.wait_stream(stream)
+                marks[i + 1].record(s_out)
 
     e_steps = max(1, min(a.steps, 5))
-    with torch.cuda.stream(stream):
-        e2e_step(stream)
-        stream.synchronize()
-        if world > 1:
-            dist.barrier()
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        c0.record(stream)
-        for _ in range(e_steps):
-            e2e_step(stream)
-        c1.record(stream)
-    stream.synchronize()
-    e_ms = max_over_ranks(c0.elapsed_time(c1), dev)
+    run_pipeline(2)                                   # warm-up (host pages, copy engines)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps + 1)]
+    with ClockSampler(local) as e_clk:
+        marks[0].record(s_in)
+        run_pipeline(e_steps, marks)
+        torch.cuda.synchronize(dev)
+    e_step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(e_steps)]
+    e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), dev)
     e2e_value = job_tflops(ff, e_steps, world, e_ms)
 
     if rank == 0:
@@ -428,7 +469,8 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu_baseline_entry(a, cpu_res) if cpu_res else None,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e_steps,
+                    "step_ms": [round(x, 2) for x in e_step_ms], "clocks": e_clk.summary()},
             "gpu_launches": int(launches),
             "clocks": clk.summary(),
             "extra": extra,

@@ -39,7 +39,7 @@ template <int D>
 struct FwdLayout {
     static constexpr int kBlocks = D / 64;                  // 128-byte column blocks
     static constexpr int kTileBytes = kTile * D * 2;        // one 128-row bf16 tile
-    static constexpr int kStages = (D == 128) ? 3 : 6;      // K/V ring depth
+    static constexpr int kStages = (D == 128) ? 4 : 6;      // K/V ring depth
     static constexpr int kQ = 0;                            // Q0, Q1
     static constexpr int kKV = 2 * kTileBytes;
     static constexpr int kBar = kKV + kStages * kTileBytes;
