@@ -10,10 +10,12 @@
 //            sequence, causal pairs, the mask: OpenWAM PR #64)
 //     dS   = P o (dP - Delta)  -> bf16, written over S_j in TMEM
 //     dQ  += dS K_j                                     (TMEM A operand)
-// Warps: 0-3 compute (thread = query row = TMEM lane; its lse2 and Delta live
-// in registers), 8 = TMA producer (Q, dO once; K_j, V_j through a ring),
-// 9 = TMEM allocator and UMMA issuer; 4-7 idle.  TMEM: S0 | S1 (double
-// buffer) | dP | dQ.  S_{j+1} is computed while the warps work on tile j.
+// Warps: 0-7 compute (thread = query row = TMEM lane; its lse2 and Delta live
+// in registers; warps 0-3 take keys 0-63 of the tile, warps 4-7 keys 64-127,
+// each half writing its packed dS over the first 32 of its own 64 S columns),
+// 8 = TMA producer (Q, dO once; K_j, V_j through a ring), 9 = TMEM allocator
+// and UMMA issuer.  TMEM: S0 | S1 (double buffer) | dP | dQ.  S_{j+1} is
+// computed while the warps work on tile j.
 #include "sm100_ptx.cuh"
 
 namespace attn {
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < L::kNumBars; ++i)
-            mbar_init(bar(i), i == L::kBarDSReady ? kT : 1);
+            mbar_init(bar(i), i == L::kBarDSReady ? 2 * kT : 1);
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -193,9 +195,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                                                    16384, 1024, kSwizzle128B);
                     const uint32_t a = tmem + ((j & 1) ? L::kColS1 : L::kColS0);
 #pragma unroll
-                    for (int kk = 0; kk < kT / 16; ++kk)
-                        mma_ts(tmem + L::kColDQ, a + kk * 8, desc_add(kmn, kk * 2048), id_dq,
-                               (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kT / 16; ++kk)    // dS of keys 16kk..: see dS_col
+                        mma_ts(tmem + L::kColDQ, a + 8 * kk + (kk >= 4 ? 32 : 0), desc_add(kmn, kk * 2048),
+                               id_dq, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(L::kBarDQDone + (j & 1)));
                 mma_commit(bar(L::kBarKVEmpty + stage(2 * j)));     // K_j consumed
@@ -216,12 +218,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
+    } else if (warp < 8) {
         // ------------------------------------------------------------ dS rows
-        const int r = warp * 32 + lane;
+        const int wq = warp & 3;                      // TMEM lane quarter
+        const int hq = warp >> 2;                     // key half of the tile (dQ: d half)
+        const int r = wq * 32 + lane;
         const int i = m0 + r;                         // query row in the sequence
         const bool row_in = i < si.len_q;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int64_t li = b * p.lse_b + h * p.lse_h + row_base + i;
         const float nl = row_in ? -p.lse2[li] : 0.f;   // -lse2 of this row
         const float dl = row_in ? p.delta[li] : 0.f;
@@ -243,7 +247,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (has_mask) {
                 // logits rewritten in TMEM chunk by chunk (mask loads would spill)
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 2 * hq; c < 2 * hq + 2; ++c) {
                     uint32_t v[32];
                     tmem_ld32(tS + 32 * c, v);
 #pragma unroll
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             }
             const int jmax = p.causal ? min(si.len_k, i + 1) : si.len_k;   // keys < jmax visible
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 2 * hq; c < 2 * hq + 2; ++c) {
                 uint32_t sv[32], dv[32];
                 tmem_ld32x2(tS + 32 * c, sv, tDP + 32 * c, dv);
                 uint32_t pk[16];
@@ -297,7 +301,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                         pk[e >> 1] = pack_bf16(ds[0], ds[1]);
                     }
                 }
-                tmem_st16(tS + 16 * c, pk);     // dS over S columns already read
+                // dS of chunk c over S columns this thread has already read:
+                // 16c (chunks 0, 1) and 32 + 16c (chunks 2, 3).
+                tmem_st16(tS + 16 * c + (c >= 2 ? 32 : 0), pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tc_fence_after();
             bf16* grow = p.dq + b * p.out_b + static_cast<int64_t>(row_base + i) * p.out_s + h * p.out_h;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = hq * (D / 64); c < (hq + 1) * (D / 64); ++c) {
                 uint32_t o[32];
                 if (n > 0) {
                     tmem_ld32(tmem + lane_off + L::kColDQ + 32 * c, o);
