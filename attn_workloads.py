@@ -5,8 +5,9 @@ parity check (the fp64 oracle and the CUDA library).  This module only draws
 random numbers and lays them out: it holds none of the attention arithmetic.
 
 Every tensor is drawn on the CPU from ``torch.Generator().manual_seed(seed)``
-in fp32 and rounded to bf16, in the fixed order q, k, v, dO, then extras, so
-both sides see the same bf16 bits.
+in fp32 and rounded to bf16 (or to fp16 when ``dtype=torch.float16``), in the
+fixed order q, k, v, dO, then extras, so both sides see the same 16-bit
+values.
 
 Workloads (sizes and value distributions as the pages give them):
 
@@ -41,22 +42,22 @@ def _randn(g, shape):
     return torch.randn(*shape, generator=g, dtype=torch.float32)
 
 
-def dense_qkvdo(B, Sq, Sk, Hq, Hkv, D, seed=42, dout="randn", k_scale=1.0):
-    """q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D], dO like q; bf16 on the CPU."""
+def dense_qkvdo(B, Sq, Sk, Hq, Hkv, D, seed=42, dout="randn", k_scale=1.0, dtype=BF16):
+    """q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D], dO like q; 16-bit on the CPU."""
     g = _gen(seed)
-    q = _randn(g, (B, Sq, Hq, D)).to(BF16)
-    k = (_randn(g, (B, Sk, Hkv, D)) * k_scale).to(BF16)
-    v = _randn(g, (B, Sk, Hkv, D)).to(BF16)
+    q = _randn(g, (B, Sq, Hq, D)).to(dtype)
+    k = (_randn(g, (B, Sk, Hkv, D)) * k_scale).to(dtype)
+    v = _randn(g, (B, Sk, Hkv, D)).to(dtype)
     if dout == "ones":
-        do = torch.ones(B, Sq, Hq, D, dtype=BF16)
+        do = torch.ones(B, Sq, Hq, D, dtype=dtype)
     else:
-        do = _randn(g, (B, Sq, Hq, D)).to(BF16)
+        do = _randn(g, (B, Sq, Hq, D)).to(dtype)
     return q, k, v, do
 
 
-def causal_small(seed=42):
+def causal_small(seed=42, dtype=BF16):
     """B=1, Hq=Hkv=1, S=256, D=64, causal, dO = ones."""
-    q, k, v, do = dense_qkvdo(1, 256, 256, 1, 1, 64, seed=seed, dout="ones")
+    q, k, v, do = dense_qkvdo(1, 256, 256, 1, 1, 64, seed=seed, dout="ones", dtype=dtype)
     return dict(q=q, k=k, v=v, do=do, causal=True, scale=1.0 / 8.0, mask=None)
 
 
@@ -89,7 +90,7 @@ def padding_mask(B, Sq, Sk, kind, Hq=1, per_row=False, seed=7):
     return add
 
 
-def low_lse_row(Sq, Sk, mask_kind, D=128, row="first", seed=42, B=2, H=4):
+def low_lse_row(Sq, Sk, mask_kind, D=128, row="first", seed=42, B=2, H=4, dtype=BF16):
     """Keys share 36 u; one query row is -36 u (row LSE far below -88.7)."""
     g = _gen(seed)
     q = _randn(g, (B, Sq, H, D))
@@ -102,13 +103,13 @@ def low_lse_row(Sq, Sk, mask_kind, D=128, row="first", seed=42, B=2, H=4):
     r = 0 if row == "first" else Sq - 1
     q[:, r, :, :] = -36.0 * u
     mask = padding_mask(B, Sq, Sk, mask_kind, Hq=H)
-    return dict(q=q.to(BF16), k=k.to(BF16), v=v.to(BF16), do=do.to(BF16),
+    return dict(q=q.to(dtype), k=k.to(dtype), v=v.to(dtype), do=do.to(dtype),
                 causal=False, scale=1.0 / math.sqrt(D), mask=mask, low_row=r)
 
 
-def wide_spread(s, B=2, S=8192, H=32, D=128, seed=42):
+def wide_spread(s, B=2, S=8192, H=32, D=128, seed=42, dtype=BF16):
     """q, v ~ N(0,1); k = bf16(N(0,1) * s); dO ~ N(0,1); non-causal."""
-    q, k, v, do = dense_qkvdo(B, S, S, H, H, D, seed=seed, k_scale=float(s))
+    q, k, v, do = dense_qkvdo(B, S, S, H, H, D, seed=seed, k_scale=float(s), dtype=dtype)
     return dict(q=q, k=k, v=v, do=do, causal=False, scale=1.0 / math.sqrt(D), mask=None)
 
 
@@ -117,7 +118,7 @@ def varlen_lengths(n=16, lo=128, hi=4096, seed=42):
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
 
 
-def varlen_gqa(n=16, lo=128, hi=4096, Hq=32, Hkv=8, D=128, trailing=512, seed=42):
+def varlen_gqa(n=16, lo=128, hi=4096, Hq=32, Hkv=8, D=128, trailing=512, seed=42, dtype=BF16):
     """Packed THD: q/dO [T,Hq,D], k/v [T,Hkv,D], cu_seqlens int32 [n+1]."""
     lens = varlen_lengths(n, lo, hi, seed)
     cu = [0]
@@ -125,16 +126,16 @@ def varlen_gqa(n=16, lo=128, hi=4096, Hq=32, Hkv=8, D=128, trailing=512, seed=42
         cu.append(cu[-1] + L)
     T = cu[-1] + trailing
     g = _gen(seed + 1)
-    q = _randn(g, (T, Hq, D)).to(BF16)
-    k = _randn(g, (T, Hkv, D)).to(BF16)
-    v = _randn(g, (T, Hkv, D)).to(BF16)
-    do = _randn(g, (T, Hq, D)).to(BF16)
+    q = _randn(g, (T, Hq, D)).to(dtype)
+    k = _randn(g, (T, Hkv, D)).to(dtype)
+    v = _randn(g, (T, Hkv, D)).to(dtype)
+    do = _randn(g, (T, Hq, D)).to(dtype)
     return dict(q=q, k=k, v=v, do=do, cu_seqlens=torch.tensor(cu, dtype=torch.int32),
                 max_seqlen=max(lens), causal=True, scale=1.0 / math.sqrt(D), lens=lens)
 
 
-def long_seq(S, causal, B=1, H=16, D=128, seed=42):
-    q, k, v, do = dense_qkvdo(B, S, S, H, H, D, seed=seed)
+def long_seq(S, causal, B=1, H=16, D=128, seed=42, dtype=BF16):
+    q, k, v, do = dense_qkvdo(B, S, S, H, H, D, seed=seed, dtype=dtype)
     return dict(q=q, k=k, v=v, do=do, causal=causal, scale=1.0 / math.sqrt(D), mask=None)
 
 

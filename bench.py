@@ -44,6 +44,8 @@ def parse(argv=None):
     ap.add_argument("--seqlen", type=int, default=131072)
     ap.add_argument("--heads", type=int, default=16)
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
+                    help="element type of q, k, v, dO and of the outputs")
     ap.add_argument("--deterministic", action="store_true",
                     help="dQ by the per-query-tile kernel instead of fp32 reductions")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -58,8 +60,9 @@ def fwd_flops(B, H, S, D, causal):
 
 
 def workload_name(a):
-    return "long_seq B=1 H=%d S=%d D=128 %s fwd+bwd%s" % (
+    return "long_seq B=1 H=%d S=%d D=128 %s%s fwd+bwd%s" % (
         a.heads, a.seqlen, "causal" if a.causal else "non-causal",
+        " fp16" if getattr(a, "dtype", "bf16") == "f16" else "",
         " (deterministic dQ)" if a.deterministic else "")
 
 
@@ -298,7 +301,7 @@ def main():
     g = torch.Generator(device=dev).manual_seed(42 + rank)
     shape = (B, S, H, D)
     q, k, v, do = (torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
-                   .to(torch.bfloat16) for _ in range(4))
+                   .to(torch.float16 if a.dtype == "f16" else torch.bfloat16) for _ in range(4))
     stream = torch.cuda.Stream(device=dev)
     ws = torch.empty(max(1, _bwd_ws(q, k)), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
@@ -459,7 +462,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms / a.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": a.dtype,
             "data": "synthetic",
             "config": {"workload": workload_name(a), "B": B, "H": H, "S": S, "D": D,
                        "causal": a.causal, "parallelism": "replicas" if world > 1 else "single",

@@ -51,7 +51,8 @@
  *              [cu[s], cu[s+1]) of q, k and v (so Sq = Sk per sequence).
  *              Rows >= cu[nseq] belong to no sequence; the library writes
  *              them as out = 0, lse = 0, dq = dk = dv = 0.
- *   Inputs q, k, v, dout, out (as a backward input): bf16, last-dim stride 1,
+ *   Inputs q, k, v, dout, out (as a backward input): bf16 or fp16 (all the
+ *   same type; it also sets the type of out, dq, dk, dv), last-dim stride 1,
  *   every other stride a multiple of 8 elements (16 bytes), base 16-byte
  *   aligned.  Outputs out, lse, dq, dk, dv: contiguous in the layouts above.
  *   Head dim D must be 64 or 128; Hq must be a multiple of Hkv (GQA).
@@ -84,7 +85,7 @@ typedef struct CUstream_st* attn_stream_t;
 /* Element types. */
 enum {
     ATTN_BF16 = 1,
-    ATTN_F16 = 2,   /* recognised so that it can be rejected: not computed */
+    ATTN_F16 = 2,   /* IEEE half: computed like bf16 (fp32 accumulation) */
     ATTN_F32 = 3,
     ATTN_I32 = 4,
     ATTN_U8 = 5     /* bool mask: nonzero = visible, 0 = hidden */
@@ -118,7 +119,7 @@ enum {
 
 typedef struct {
     void* data;          /* device pointer */
-    int32_t dtype;       /* ATTN_BF16, ATTN_F32, ATTN_I32, ATTN_U8, ... */
+    int32_t dtype;       /* ATTN_BF16, ATTN_F16, ATTN_F32, ATTN_I32, ATTN_U8 */
     int32_t ndim;        /* 1 .. 4 */
     int64_t shape[4];
     int64_t stride[4];   /* in elements; 0 = broadcast (masks only) */
@@ -128,17 +129,20 @@ typedef struct {
 /*
  * attn_fwd - forward pass: out and lse.
  *
- *   q, k, v     bf16 inputs (dense [B,S,H,D] or varlen [T,H,D]).
+ *   q, k, v     bf16 or fp16 inputs, all three the same type (dense
+ *               [B,S,H,D] or varlen [T,H,D]); any other type or a mix gives
+ *               ATTN_E_DTYPE before anything is launched.
  *   mask        NULL, or a dense-only mask broadcastable to [B,Hq,Sq,Sk]
  *               (rank 4, stride 0 on broadcast axes): ATTN_U8 (bool,
- *               0 = hidden), ATTN_F32 or ATTN_BF16 (additive, -inf = hidden).
+ *               0 = hidden), ATTN_F32, ATTN_BF16 or ATTN_F16 (additive,
+ *               -inf = hidden).
  *               The mask is added after scaling.
  *   cu_seqlens  NULL for dense, else int32 [nseq+1] on the device (varlen).
  *   max_seqlen  varlen only: an upper bound on every sequence length (a
  *               longer sequence is skipped and flagged ATTN_E_SEQLENS).
  *   causal      nonzero = causal (top-left).
  *   scale       finite softmax scale (callers usually pass 1/sqrt(D)).
- *   out         bf16, same shape as q, contiguous; fully written.
+ *   out         q's element type, same shape as q, contiguous; fully written.
  *   lse         fp32 [B,Hq,Sq] (dense) or [Hq,T] (varlen), contiguous; fully
  *               written, natural log.
  *   flags       0 or ATTN_EAGER_RESCALE.
@@ -161,7 +165,7 @@ size_t attn_bwd_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* k, 
  *
  *   q, k, v, out, dout, lse   as produced / consumed by attn_fwd with the
  *               same mask, cu_seqlens, max_seqlen, causal and scale.
- *   dq, dk, dv  bf16, shapes of q, k, v, contiguous; fully written (the
+ *   dq, dk, dv  q's element type, shapes of q, k, v, contiguous; fully written (the
  *               caller may pass uninitialised memory).
  *   workspace   device buffer of at least attn_bwd_workspace_bytes() bytes,
  *               256-byte aligned; contents on entry are ignored (it is

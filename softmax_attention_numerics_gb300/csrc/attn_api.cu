@@ -6,7 +6,8 @@
 // input-validation holes ..."): every companion tensor is checked against
 // the shape contract derived from q (a transposed dout or lse must fail, not
 // run), all tensors sit on one device, the dtype gate matches what the
-// kernels compute (bf16 only; fp16 is rejected, never reinterpreted), and
+// kernels compute (bf16 or fp16, templated on the element type and never
+// reinterpreted: q, k, v, out, dout, dq, dk, dv must all have q's type), and
 // out-parameters must be contiguous.  Unsupported head dims are rejected
 // before launch (PFCCLab/cudnn-frontend PR #9, section 4).
 #include <atomic>
@@ -65,11 +66,11 @@ int run_stage(int stage, cudaStream_t st, F&& launch) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// bf16 input: rank r, last stride 1, other strides multiples of 8 elements
-// (for dims longer than 1), 16-byte aligned base.
-int check_input(const attn_tensor_t* t, int rank) {
+// 16-bit input of element type `dtype`: rank r, last stride 1, other strides
+// multiples of 8 elements (for dims longer than 1), 16-byte aligned base.
+int check_input(const attn_tensor_t* t, int rank, int dtype) {
     if (!t) return ATTN_E_ARG;
-    if (t->dtype != ATTN_BF16) return ATTN_E_DTYPE;
+    if (t->dtype != dtype) return ATTN_E_DTYPE;
     if (t->ndim != rank) return ATTN_E_SHAPE;
     int64_t n = 1;
     for (int i = 0; i < rank; ++i) {
@@ -130,6 +131,7 @@ int check_device(const attn_tensor_t* t, int dev) {
 // Shape contract derived from q and k; fills the shape-related fields of p.
 struct Shapes {
     int varlen;
+    int elt;        // ATTN_BF16 or ATTN_F16: the element type of q and every 16-bit tensor
     int64_t B, Sq, Sk, Hq, Hkv, D, T, nseq;
     int64_t q_shape[4], k_shape[4], lse_shape[3];
     int rank, lse_rank;
@@ -140,12 +142,14 @@ int derive_shapes(const attn_tensor_t* q, const attn_tensor_t* k, const attn_ten
     s->varlen = cu != nullptr;
     s->rank = s->varlen ? 3 : 4;
     if (!q || !k || !v) return ATTN_E_ARG;
-    if (q->dtype == ATTN_F16 || k->dtype == ATTN_F16 || v->dtype == ATTN_F16) return ATTN_E_DTYPE;
+    // bf16 or fp16, the same for q, k, v (and for out, dout, dq, dk, dv).
+    if (q->dtype != ATTN_BF16 && q->dtype != ATTN_F16) return ATTN_E_DTYPE;
+    s->elt = q->dtype;
     if (q->ndim == s->rank && q->shape[s->rank - 1] != 64 && q->shape[s->rank - 1] != 128)
         return ATTN_E_UNSUPPORTED;
-    ATTN_TRY(check_input(q, s->rank));
-    ATTN_TRY(check_input(k, s->rank));
-    ATTN_TRY(check_input(v, s->rank));
+    ATTN_TRY(check_input(q, s->rank, s->elt));
+    ATTN_TRY(check_input(k, s->rank, s->elt));
+    ATTN_TRY(check_input(v, s->rank, s->elt));
     if (s->varlen) {
         s->T = q->shape[0];
         s->Hq = q->shape[1];
@@ -226,6 +230,7 @@ int fill_common(Problem* p, const Shapes& s, const attn_tensor_t* q, const attn_
     p->Sq = static_cast<int>(s.Sq);
     p->Sk = static_cast<int>(s.Sk);
     p->D = static_cast<int>(s.D);
+    p->f16 = s.elt == ATTN_F16 ? 1 : 0;
     p->varlen = s.varlen;
     p->cu = s.varlen ? static_cast<const int*>(cu->data) : nullptr;
     p->T = static_cast<int>(s.T);
@@ -268,6 +273,8 @@ int fill_common(Problem* p, const Shapes& s, const attn_tensor_t* q, const attn_
             p->mask_kind = MASK_F32;
         else if (mask->dtype == ATTN_BF16)
             p->mask_kind = MASK_BF16;
+        else if (mask->dtype == ATTN_F16)
+            p->mask_kind = MASK_F16;
         else
             return ATTN_E_DTYPE;
         p->mask = mask->data;
@@ -329,7 +336,7 @@ extern "C" int attn_fwd(const attn_tensor_t* q, const attn_tensor_t* k, const at
                         attn_tensor_t* lse, uint32_t flags, attn_stream_t stream) {
     Shapes s;
     ATTN_TRY(derive_shapes(q, k, v, cu_seqlens, max_seqlen, &s));
-    ATTN_TRY(check_output(out, ATTN_BF16, s.q_shape, s.rank));
+    ATTN_TRY(check_output(out, s.elt, s.q_shape, s.rank));
     ATTN_TRY(check_output(lse, ATTN_F32, s.lse_shape, s.lse_rank));
     Problem p;
     ATTN_TRY(fill_common(&p, s, q, k, v, mask, cu_seqlens, causal, scale, flags));
@@ -375,17 +382,16 @@ extern "C" int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const at
     Shapes s;
     ATTN_TRY(derive_shapes(q, k, v, cu_seqlens, max_seqlen, &s));
     if (!out || !dout || !lse) return ATTN_E_ARG;
-    if (out->dtype == ATTN_F16 || dout->dtype == ATTN_F16) return ATTN_E_DTYPE;
-    ATTN_TRY(check_input(out, s.rank));
-    ATTN_TRY(check_input(dout, s.rank));
+    ATTN_TRY(check_input(out, s.rank, s.elt));
+    ATTN_TRY(check_input(dout, s.rank, s.elt));
     if (!same_shape(out, s.q_shape, s.rank) || !same_shape(dout, s.q_shape, s.rank))
         return ATTN_E_SHAPE;
     if (lse->dtype != ATTN_F32) return ATTN_E_DTYPE;
     if (!same_shape(lse, s.lse_shape, s.lse_rank)) return ATTN_E_SHAPE;
     if (!is_contiguous(lse)) return ATTN_E_LAYOUT;
-    ATTN_TRY(check_output(dq, ATTN_BF16, s.q_shape, s.rank));
-    ATTN_TRY(check_output(dk, ATTN_BF16, s.k_shape, s.rank));
-    ATTN_TRY(check_output(dv, ATTN_BF16, s.k_shape, s.rank));
+    ATTN_TRY(check_output(dq, s.elt, s.q_shape, s.rank));
+    ATTN_TRY(check_output(dk, s.elt, s.k_shape, s.rank));
+    ATTN_TRY(check_output(dv, s.elt, s.k_shape, s.rank));
     const WsLayout w = ws_layout(s, flags);
     if (w.total > 0) {
         if (!workspace) return ATTN_E_WORKSPACE;
@@ -439,7 +445,7 @@ extern "C" int attn_get_error(attn_stream_t stream) {
 extern "C" const char* attn_strerror(int code) {
     switch (code) {
         case ATTN_OK: return "ok";
-        case ATTN_E_DTYPE: return "unsupported element type (bf16 inputs only; fp16 is rejected)";
+        case ATTN_E_DTYPE: return "unsupported or mismatched element type (bf16 or fp16 inputs, all alike; fp32 lse)";
         case ATTN_E_SHAPE: return "shape does not match the contract derived from q";
         case ATTN_E_LAYOUT: return "stride, alignment or contiguity violation";
         case ATTN_E_DEVICE: return "tensors are not all on the current CUDA device";

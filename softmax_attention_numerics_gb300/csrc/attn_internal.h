@@ -4,14 +4,17 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace attn {
 
+// 16-bit element storage.  The pointers below are typed bf16 for both
+// element types; `f16` says how the bits are read (bf16 or IEEE fp16).
 typedef __nv_bfloat16 bf16;
 
-enum MaskKind { MASK_NONE = 0, MASK_BOOL = 1, MASK_F32 = 2, MASK_BF16 = 3 };
+enum MaskKind { MASK_NONE = 0, MASK_BOOL = 1, MASK_F32 = 2, MASK_BF16 = 3, MASK_F16 = 4 };
 
 // Every stride is in elements.  Row addressing for a (batch b, head h, row i
 // of that batch/sequence) is  ptr + b * x_b + (row0(b) + i) * x_s + h * x_h,
@@ -45,6 +48,7 @@ struct Problem {
     int Hq, Hkv, G; // G = Hq / Hkv
     int Sq, Sk;     // dense lengths; varlen: max_seqlen for both
     int D;
+    int f16;        // 1: q, k, v, out, dout, dq, dk, dv hold fp16; 0: bf16
     int varlen;
     const int* cu;  // varlen: int32 [B + 1]
     int T;          // varlen: total rows of q/k/v
@@ -65,11 +69,11 @@ constexpr int DEV_E_TIMEOUT = -8;
 constexpr int DEV_E_SEQLENS = -9;
 constexpr int DEV_E_INTERNAL = -11;
 
-// TMA tensor map over a bf16 [B, S, H, D] view (dims innermost first: D, H,
-// S, B; strides in elements), box 64 x 1 x 128 x 1, 128-byte swizzle.
-// Rows past S read as zero and are clipped on store.
+// TMA tensor map over a 16-bit (bf16, or fp16 when f16) [B, S, H, D] view
+// (dims innermost first: D, H, S, B; strides in elements), box 64 x 1 x 128 x 1,
+// 128-byte swizzle.  Rows past S read as zero and are clipped on store.
 bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t S, int64_t B,
-                   int64_t sh, int64_t ss, int64_t sb);
+                   int64_t sh, int64_t ss, int64_t sb, bool f16);
 
 // TMA tensor map over the fp32 dQ workspace [R, H, D] (dims D, H, R), box
 // 32 x 1 x 128, 128-byte swizzle; the target of bulk reduce-adds.

@@ -1,6 +1,6 @@
 // Memory-bound helper kernels of the backward and the varlen tails:
 //   bwd_preprocess  Delta = rowsum(dO o O) in fp32 and lse2 = lse * log2(e)
-//   dq_convert      dq = bf16(dq_acc * scale)
+//   dq_convert      dq = bf16 / fp16 (dq_acc * scale)
 //   zero_trailing   rows >= cu[nseq] of a packed varlen buffer: out = 0 and
 //                   lse = 0 (forward), dq = dk = dv = 0 (backward).  Rows that no
 //                   tile visits must still be written (PFCCLab/cudnn-frontend
@@ -12,7 +12,7 @@ namespace attn {
 namespace {
 
 // One warp per (row, head); D/32 elements per lane.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256) preprocess_kernel(const Problem p, int64_t rows) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -36,20 +36,17 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const Problem p, int64_
         if (D == 128) {
             const uint2 ov = *reinterpret_cast<const uint2*>(og + lane * 4);
             const uint2 dv = *reinterpret_cast<const uint2*>(dg + lane * 4);
-            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-            const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+            const uint32_t ow[2] = {ov.x, ov.y}, dw[2] = {dv.x, dv.y};
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const float2 a = __bfloat1622float2(o2[e]);
-                const float2 c = __bfloat1622float2(d2[e]);
+                const float2 a = unpack2<F16>(ow[e]);
+                const float2 c = unpack2<F16>(dw[e]);
                 acc = fmaf(a.x, c.x, acc);
                 acc = fmaf(a.y, c.y, acc);
             }
         } else {
-            const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(og + lane * 2);
-            const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(dg + lane * 2);
-            const float2 a = __bfloat1622float2(o2);
-            const float2 c = __bfloat1622float2(d2);
+            const float2 a = unpack2<F16>(*reinterpret_cast<const uint32_t*>(og + lane * 2));
+            const float2 c = unpack2<F16>(*reinterpret_cast<const uint32_t*>(dg + lane * 2));
             acc = fmaf(a.x, c.x, acc);
             acc = fmaf(a.y, c.y, acc);
         }
@@ -63,7 +60,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const Problem p, int64_
     }
 }
 
-// dq = bf16(acc * scale), 4 elements per thread-iteration.
+// dq = 16-bit(acc * scale), 4 elements per thread-iteration.
+template <bool F16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
                                                          bf16* __restrict__ dq, int64_t n4,
                                                          float scale) {
@@ -72,8 +70,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
          i += stride) {
         const float4 a = reinterpret_cast<const float4*>(acc)[i];
         uint2 o;
-        o.x = pack_bf16(a.x * scale, a.y * scale);
-        o.y = pack_bf16(a.z * scale, a.w * scale);
+        o.x = pack2<F16>(a.x * scale, a.y * scale);
+        o.y = pack2<F16>(a.z * scale, a.w * scale);
         reinterpret_cast<uint2*>(dq)[i] = o;
     }
 }
@@ -85,7 +83,7 @@ __device__ __forceinline__ int64_t trailing_start(const Problem& p) {
     return e;
 }
 
-// Zero rows [cu[B], T) of a contiguous [T, H, D] bf16 buffer (8 elems per op).
+// Zero rows [cu[B], T) of a contiguous [T, H, D] 16-bit buffer (8 elems per op).
 __device__ __forceinline__ void zero_rows_bf16(bf16* base, int64_t r0, int64_t T, int H, int D) {
     const int64_t per_row = static_cast<int64_t>(H) * D / 8;
     const int64_t n = (T - r0) * per_row;
@@ -133,10 +131,17 @@ cudaError_t launch_bwd_preprocess(const Problem& p, cudaStream_t stream) {
     const int64_t rows = p.varlen ? p.T : static_cast<int64_t>(p.B) * p.Sq;
     if (rows == 0) return cudaSuccess;
     const int blocks = grid_for(rows * p.Hq * 32, 256);
-    if (p.D == 64)
-        preprocess_kernel<64><<<blocks, 256, 0, stream>>>(p, rows);
-    else
-        preprocess_kernel<128><<<blocks, 256, 0, stream>>>(p, rows);
+    if (p.f16) {
+        if (p.D == 64)
+            preprocess_kernel<64, true><<<blocks, 256, 0, stream>>>(p, rows);
+        else
+            preprocess_kernel<128, true><<<blocks, 256, 0, stream>>>(p, rows);
+    } else {
+        if (p.D == 64)
+            preprocess_kernel<64, false><<<blocks, 256, 0, stream>>>(p, rows);
+        else
+            preprocess_kernel<128, false><<<blocks, 256, 0, stream>>>(p, rows);
+    }
     return cudaGetLastError();
 }
 
@@ -144,7 +149,10 @@ cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream) {
     const int64_t rows = p.varlen ? p.T : static_cast<int64_t>(p.B) * p.Sq;
     const int64_t n4 = rows * p.Hq * p.D / 4;
     if (n4 == 0) return cudaSuccess;
-    dq_convert_kernel<<<grid_for(n4, 256), 256, 0, stream>>>(p.dq_acc, p.dq, n4, p.scale);
+    if (p.f16)
+        dq_convert_kernel<true><<<grid_for(n4, 256), 256, 0, stream>>>(p.dq_acc, p.dq, n4, p.scale);
+    else
+        dq_convert_kernel<false><<<grid_for(n4, 256), 256, 0, stream>>>(p.dq_acc, p.dq, n4, p.scale);
     return cudaGetLastError();
 }
 

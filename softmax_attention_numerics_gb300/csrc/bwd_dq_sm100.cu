@@ -55,7 +55,7 @@ struct DqMaps {
     CUtensorMap q, dout, k, v;
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_sm100_kernel(const Problem p, const __grid_constant__ DqMaps maps) {
     using L = DqLayout<D>;
@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------------ UMMA issuer
         if (lane == 0) {
-            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);    // S, dP (K-major)
-            constexpr uint32_t id_dq = idesc_bf16(128, D, 0, 1);     // dQ += dS K (B MN-major)
+            constexpr uint32_t id_s = idesc_f16kind(128, 128, 0, 0, F16);    // S, dP (K-major)
+            constexpr uint32_t id_dq = idesc_f16kind(128, D, 0, 1, F16);     // dQ += dS K (B MN-major)
             const uint64_t q_k = smem_desc(sbase + L::kQ, 16, 1024, kSwizzle128B);
             const uint64_t do_k = smem_desc(sbase + L::kDO, 16, 1024, kSwizzle128B);
             auto stage = [&](int li) { return li % L::kStages; };
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                         const float2 d2 = fadd2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
                                                 nd2);
                         const float2 ds2 = fmul2(make_float2(p0, p1), d2);
-                        pk[e >> 1] = pack_bf16(ds2.x, ds2.y);
+                        pk[e >> 1] = pack2<F16>(ds2.x, ds2.y);
                     }
                 } else {
 #pragma unroll
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                             const float pv = ex2(fminf(x + nl, 0.f));
                             ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) - dl) : 0.f;
                         }
-                        pk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                        pk[e >> 1] = pack2<F16>(ds[0], ds[1]);
                     }
                 }
                 // dS of chunk c over S columns this thread has already read:
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * p.scale,
+                        pk[e] = pack2<F16>(__uint_as_float(o[2 * e]) * p.scale,
                                           __uint_as_float(o[2 * e + 1]) * p.scale);
                     uint4* dst = reinterpret_cast<uint4*>(grow + 32 * c);
 #pragma unroll
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (tid == 0 && *abort_flag) set_error(p.err, DEV_E_TIMEOUT);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_dq_sm100_d(const Problem& p, cudaStream_t stream) {
     using L = DqLayout<D>;
     if (p.B == 0 || p.Sq == 0) return cudaSuccess;
@@ -360,25 +360,27 @@ cudaError_t launch_dq_sm100_d(const Problem& p, cudaStream_t stream) {
     const bool no_keys = Sk == 0;    // maps must stay legal; they are never read then
     DqMaps maps;
     const bool ok =
-        make_tile_map(&maps.q, p.q, D, p.Hq, Sq, Bm, p.q_h, p.q_s, p.q_b) &&
-        make_tile_map(&maps.dout, p.dout, D, p.Hq, Sq, Bm, p.do_h, p.do_s, p.do_b) &&
+        make_tile_map(&maps.q, p.q, D, p.Hq, Sq, Bm, p.q_h, p.q_s, p.q_b, F16) &&
+        make_tile_map(&maps.dout, p.dout, D, p.Hq, Sq, Bm, p.do_h, p.do_s, p.do_b, F16) &&
         make_tile_map(&maps.k, no_keys ? p.q : p.k, D, no_keys ? p.Hq : p.Hkv, no_keys ? Sq : Sk, Bm,
-                      no_keys ? p.q_h : p.k_h, no_keys ? p.q_s : p.k_s, no_keys ? p.q_b : p.k_b) &&
+                      no_keys ? p.q_h : p.k_h, no_keys ? p.q_s : p.k_s, no_keys ? p.q_b : p.k_b, F16) &&
         make_tile_map(&maps.v, no_keys ? p.q : p.v, D, no_keys ? p.Hq : p.Hkv, no_keys ? Sq : Sk, Bm,
-                      no_keys ? p.q_h : p.v_h, no_keys ? p.q_s : p.v_s, no_keys ? p.q_b : p.v_b);
+                      no_keys ? p.q_h : p.v_h, no_keys ? p.q_s : p.v_s, no_keys ? p.q_b : p.v_b, F16);
     if (!ok) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(bwd_dq_sm100_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_sm100_kernel<D, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((p.Sq + kT - 1) / kT, p.Hq, p.B);
-    bwd_dq_sm100_kernel<D><<<grid, kDqThreads, L::kBytes, stream>>>(p, maps);
+    bwd_dq_sm100_kernel<D, F16><<<grid, kDqThreads, L::kBytes, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dq_deterministic(const Problem& p, cudaStream_t stream) {
-    return p.D == 64 ? launch_dq_sm100_d<64>(p, stream) : launch_dq_sm100_d<128>(p, stream);
+    if (p.f16)
+        return p.D == 64 ? launch_dq_sm100_d<64, true>(p, stream) : launch_dq_sm100_d<128, true>(p, stream);
+    return p.D == 64 ? launch_dq_sm100_d<64, false>(p, stream) : launch_dq_sm100_d<128, false>(p, stream);
 }
 
 }  // namespace attn

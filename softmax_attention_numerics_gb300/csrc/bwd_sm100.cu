@@ -89,7 +89,7 @@ __device__ __forceinline__ void stage_row_chunk(uint8_t* tile, int row, int col0
     }
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem p, const __grid_constant__ BwdMaps maps,
                                                   int with_dq) {
     using L = BwdLayout<D>;
@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ UMMA issuer
         if (lane == 0) {
-            constexpr uint32_t id_sdp = idesc_bf16(128, 128, 0, 0);    // S^T, dP^T
-            constexpr uint32_t id_acc = idesc_bf16(128, D, 0, 1);      // dV, dK (B MN-major)
-            constexpr uint32_t id_dq = idesc_bf16(128, D, 1, 1);       // dQ (A, B MN-major)
+            constexpr uint32_t id_sdp = idesc_f16kind(128, 128, 0, 0, F16);    // S^T, dP^T
+            constexpr uint32_t id_acc = idesc_f16kind(128, D, 0, 1, F16);      // dV, dK (B MN-major)
+            constexpr uint32_t id_dq = idesc_f16kind(128, D, 1, 1, F16);       // dQ (A, B MN-major)
             const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP;
             const uint32_t tDV = tmem + L::kColDV, tDK = tmem + L::kColDK;
             const uint64_t k_k = smem_desc(sbase + L::kK, 16, 1024, kSwizzle128B);
@@ -382,8 +382,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                             const float2 d2 = fadd2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
                                                     nd2);
                             const float2 ds2 = fmul2(make_float2(p0, p1), d2);
-                            pk[e >> 1] = pack_bf16(p0, p1);
-                            dk[e >> 1] = pack_bf16(ds2.x, ds2.y);
+                            pk[e >> 1] = pack2<F16>(p0, p1);
+                            dk[e >> 1] = pack2<F16>(ds2.x, ds2.y);
                             if ((e & 3) == 2) {
                                 lv = lvn;
                                 dl = dln;
@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                                 pr[u] = vis ? pv : 0.f;
                                 ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) + nd) : 0.f;
                             }
-                            pk[e >> 1] = pack_bf16(pr[0], pr[1]);
-                            dk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                            pk[e >> 1] = pack2<F16>(pr[0], pr[1]);
+                            dk[e >> 1] = pack2<F16>(ds[0], ds[1]);
                         }
                     } else {
                         // mask: S^T already holds the finished log2-domain logits
@@ -423,8 +423,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                                 pr[u] = vis ? pv : 0.f;
                                 ds[u] = vis ? pv * (__uint_as_float(dv[e + u]) + nd) : 0.f;
                             }
-                            pk[e >> 1] = pack_bf16(pr[0], pr[1]);
-                            dk[e >> 1] = pack_bf16(ds[0], ds[1]);
+                            pk[e >> 1] = pack2<F16>(pr[0], pr[1]);
+                            dk[e >> 1] = pack2<F16>(ds[0], ds[1]);
                         }
                     }
                     tmem_st16(tS + 32 * c, pk);
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * mul,
+                    pk[e] = pack2<F16>(__uint_as_float(o[2 * e]) * mul,
                                       __uint_as_float(o[2 * e + 1]) * mul);
                 if (!ok) {
                 } else if (tma_path) {
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
 
 // ------------------------------------------------------------------ host side
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_bwd_sm100_d(const Problem& p, bool with_dq, cudaStream_t stream) {
     using L = BwdLayout<D>;
     if (p.B == 0 || p.Sk == 0) return cudaSuccess;
@@ -552,14 +552,14 @@ cudaError_t launch_bwd_sm100_d(const Problem& p, bool with_dq, cudaStream_t stre
     // With no queries the maps are never read; keep them legal by pointing at k.
     const bool no_q = Sq == 0;
     BwdMaps maps;
-    bool ok = make_tile_map(&maps.k, p.k, D, p.Hkv, Sk, Bm, p.k_h, p.k_s, p.k_b) &&
-              make_tile_map(&maps.v, p.v, D, p.Hkv, Sk, Bm, p.v_h, p.v_s, p.v_b) &&
+    bool ok = make_tile_map(&maps.k, p.k, D, p.Hkv, Sk, Bm, p.k_h, p.k_s, p.k_b, F16) &&
+              make_tile_map(&maps.v, p.v, D, p.Hkv, Sk, Bm, p.v_h, p.v_s, p.v_b, F16) &&
               make_tile_map(&maps.q, no_q ? p.k : p.q, D, no_q ? p.Hkv : p.Hq, no_q ? Sk : Sq, Bm,
-                       no_q ? p.k_h : p.q_h, no_q ? p.k_s : p.q_s, no_q ? p.k_b : p.q_b) &&
+                       no_q ? p.k_h : p.q_h, no_q ? p.k_s : p.q_s, no_q ? p.k_b : p.q_b, F16) &&
               make_tile_map(&maps.dout, no_q ? p.k : p.dout, D, no_q ? p.Hkv : p.Hq, no_q ? Sk : Sq, Bm,
-                       no_q ? p.k_h : p.do_h, no_q ? p.k_s : p.do_s, no_q ? p.k_b : p.do_b) &&
-              make_tile_map(&maps.dk, p.dk, D, p.Hkv, Sk, Bm, p.dk_h, p.dk_s, p.dk_b) &&
-              make_tile_map(&maps.dv, p.dv, D, p.Hkv, Sk, Bm, p.dk_h, p.dk_s, p.dk_b);
+                       no_q ? p.k_h : p.do_h, no_q ? p.k_s : p.do_s, no_q ? p.k_b : p.do_b, F16) &&
+              make_tile_map(&maps.dk, p.dk, D, p.Hkv, Sk, Bm, p.dk_h, p.dk_s, p.dk_b, F16) &&
+              make_tile_map(&maps.dv, p.dv, D, p.Hkv, Sk, Bm, p.dk_h, p.dk_s, p.dk_b, F16);
     if (with_dq) {
         const int64_t rows = p.varlen ? p.T : static_cast<int64_t>(p.B) * p.Sq;
         ok = ok && make_f32_reduce_map(&maps.dq_acc, p.dq_acc, D, p.Hq, rows);
@@ -567,19 +567,22 @@ cudaError_t launch_bwd_sm100_d(const Problem& p, bool with_dq, cudaStream_t stre
         maps.dq_acc = maps.k;   // never read without dQ
     }
     if (!ok) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(bwd_sm100_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_sm100_kernel<D, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((p.Sk + kT - 1) / kT, p.Hkv, p.B);
-    bwd_sm100_kernel<D><<<grid, kBwdThreads, L::kBytes, stream>>>(p, maps, with_dq ? 1 : 0);
+    bwd_sm100_kernel<D, F16><<<grid, kBwdThreads, L::kBytes, stream>>>(p, maps, with_dq ? 1 : 0);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_main(const Problem& p, bool with_dq_atomics, cudaStream_t stream) {
-    return p.D == 64 ? launch_bwd_sm100_d<64>(p, with_dq_atomics, stream)
-                     : launch_bwd_sm100_d<128>(p, with_dq_atomics, stream);
+    if (p.f16)
+        return p.D == 64 ? launch_bwd_sm100_d<64, true>(p, with_dq_atomics, stream)
+                         : launch_bwd_sm100_d<128, true>(p, with_dq_atomics, stream);
+    return p.D == 64 ? launch_bwd_sm100_d<64, false>(p, with_dq_atomics, stream)
+                     : launch_bwd_sm100_d<128, false>(p, with_dq_atomics, stream);
 }
 
 }  // namespace attn

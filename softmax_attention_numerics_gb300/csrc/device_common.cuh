@@ -1,5 +1,5 @@
 // Device helpers shared by the attention kernels: sequence bounds, mask and
-// predicate evaluation, exp2 / log2 and bf16 packing.
+// predicate evaluation, exp2 / log2 and 16-bit packing.
 #pragma once
 
 #include <math.h>
@@ -75,6 +75,8 @@ __device__ __forceinline__ float mask_log2(const Problem& p, int b, int h, int i
         return static_cast<const uint8_t*>(p.mask)[off] ? 0.0f : -INFINITY;
     } else if (p.mask_kind == MASK_F32) {
         return static_cast<const float*>(p.mask)[off] * kLog2e;
+    } else if (p.mask_kind == MASK_F16) {
+        return __half2float(static_cast<const __half*>(p.mask)[off]) * kLog2e;
     } else {
         return __bfloat162float(static_cast<const bf16*>(p.mask)[off]) * kLog2e;
     }
@@ -92,9 +94,28 @@ __device__ __forceinline__ float logit_log2(const Problem& p, float acc, int b, 
     return x;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
+// Two floats -> one 32-bit word of two 16-bit elements (lo in the low half),
+// round to nearest even: bf16, or fp16 when F16.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    if constexpr (F16) {
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    } else {
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    }
+    return r;
+}
+
+// The two 16-bit elements of a packed word as floats (lo, hi).
+template <bool F16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (F16) {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w);
+        return __half22float2(h);
+    } else {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
 }
 
 }  // namespace attn

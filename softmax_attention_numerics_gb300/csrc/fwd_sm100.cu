@@ -62,7 +62,7 @@ struct FwdMaps {
     CUtensorMap q, k, v;
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_sm100_kernel(const Problem p, const __grid_constant__ FwdMaps maps) {
     using L = FwdLayout<D>;
@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------------ UMMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
+            constexpr uint32_t idesc_qk = idesc_f16kind(128, 128, 0, 0, F16);
+            constexpr uint32_t idesc_pv = idesc_f16kind(128, D, 0, 1, F16);
             const uint32_t colS[2] = {L::kColS0, L::kColS1};
             const uint32_t colO[2] = {L::kColO0, L::kColO1};
             auto kv_stage = [&](int li) { return li % L::kStages; };
@@ -333,9 +333,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     p2.x = ex2(fminf(d2.x, kLazyTau));
                     p2.y = ex2(fminf(d2.y, kLazyTau));
                     l2 = fadd2(l2, p2);
-                    pk[e] = pack_bf16(p2.x, p2.y);
-                    lr2 = fadd2(lr2, make_float2(__uint_as_float(pk[e] << 16),
-                                                 __uint_as_float(pk[e] & 0xffff0000u)));
+                    pk[e] = pack2<F16>(p2.x, p2.y);
+                    lr2 = fadd2(lr2, unpack2<F16>(pk[e]));
                 }
                 tmem_st16(tS + 16 * c, pk);
             }
@@ -384,7 +383,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv,
+                        pk[e] = pack2<F16>(__uint_as_float(o[2 * e]) * inv,
                                           __uint_as_float(o[2 * e + 1]) * inv);
                     uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
@@ -409,7 +408,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_fwd_sm100_d(const Problem& p, cudaStream_t stream) {
     using L = FwdLayout<D>;
     if (p.B == 0 || p.Sq == 0) return cudaSuccess;
@@ -419,25 +418,27 @@ cudaError_t launch_fwd_sm100_d(const Problem& p, cudaStream_t stream) {
     const int64_t Bm = p.varlen ? 1 : p.B;
     // An empty key set still needs legal maps; point them at q.
     const bool no_keys = Sk == 0;
-    if (!make_tile_map(&maps.q, p.q, D, p.Hq, S, Bm, p.q_h, p.q_s, p.q_b)) return cudaErrorInvalidValue;
+    if (!make_tile_map(&maps.q, p.q, D, p.Hq, S, Bm, p.q_h, p.q_s, p.q_b, F16)) return cudaErrorInvalidValue;
     if (!make_tile_map(&maps.k, no_keys ? p.q : p.k, D, no_keys ? p.Hq : p.Hkv, no_keys ? S : Sk, Bm,
-                  no_keys ? p.q_h : p.k_h, no_keys ? p.q_s : p.k_s, no_keys ? p.q_b : p.k_b))
+                  no_keys ? p.q_h : p.k_h, no_keys ? p.q_s : p.k_s, no_keys ? p.q_b : p.k_b, F16))
         return cudaErrorInvalidValue;
     if (!make_tile_map(&maps.v, no_keys ? p.q : p.v, D, no_keys ? p.Hq : p.Hkv, no_keys ? S : Sk, Bm,
-                  no_keys ? p.q_h : p.v_h, no_keys ? p.q_s : p.v_s, no_keys ? p.q_b : p.v_b))
+                  no_keys ? p.q_h : p.v_h, no_keys ? p.q_s : p.v_s, no_keys ? p.q_b : p.v_b, F16))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(fwd_sm100_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(fwd_sm100_kernel<D, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((p.Sq + 2 * kTile - 1) / (2 * kTile), p.Hq, p.B);
-    fwd_sm100_kernel<D><<<grid, kFwdThreads, L::kBytes, stream>>>(p, maps);
+    fwd_sm100_kernel<D, F16><<<grid, kFwdThreads, L::kBytes, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const Problem& p, cudaStream_t stream) {
-    return p.D == 64 ? launch_fwd_sm100_d<64>(p, stream) : launch_fwd_sm100_d<128>(p, stream);
+    if (p.f16)
+        return p.D == 64 ? launch_fwd_sm100_d<64, true>(p, stream) : launch_fwd_sm100_d<128, true>(p, stream);
+    return p.D == 64 ? launch_fwd_sm100_d<64, false>(p, stream) : launch_fwd_sm100_d<128, false>(p, stream);
 }
 
 }  // namespace attn

@@ -331,12 +331,13 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
     return d + static_cast<uint64_t>(bytes >> 4);
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulate.
+// Instruction descriptor for kind::f16 with fp32 accumulate and A, B both
+// bf16 (f16 = false) or both fp16 (f16 = true).
 // a_mn / b_mn: operand stored MN-major (transposed) instead of K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, int a_mn, int b_mn, bool f16) {
     return (1u << 4)                                   // D format: f32
-           | (1u << 7)                                 // A format: bf16
-           | (1u << 10)                                // B format: bf16
+           | ((f16 ? 0u : 1u) << 7)                    // A format: fp16 0, bf16 1
+           | ((f16 ? 0u : 1u) << 10)                   // B format: fp16 0, bf16 1
            | (static_cast<uint32_t>(a_mn) << 15)       // A major
            | (static_cast<uint32_t>(b_mn) << 16)       // B major
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8

@@ -28,7 +28,7 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t S, int64_t B,
-                   int64_t sh, int64_t ss, int64_t sb) {
+                   int64_t sh, int64_t ss, int64_t sb, bool f16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
@@ -38,7 +38,8 @@ bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64
     if (B == 1) strides[2] = strides[1] * (cuuint64_t)(S > 0 ? S : 1);
     cuuint32_t box[4] = {64, 1, 128, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+              const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;

@@ -90,13 +90,40 @@ def call_bwd(lib, t, mask=None, cu=None, max_seqlen=0, ws=FAKE, ws_bytes=1 << 40
                         ctypes.c_void_p(ws), ws_bytes, flags, None)
 
 
-def test_rejects_fp16(lib):
+def test_rejects_mixed_or_unsupported_element_types(lib):
+    # fp16 is computed, but every 16-bit tensor must have q's type
     t = dense()
     t["q"] = desc([2, 100, 4, 128], _lib.ATTN_F16)
-    assert call_fwd(lib, t) == E["ATTN_E_DTYPE"]
+    assert call_fwd(lib, t) == E["ATTN_E_DTYPE"]                 # k, v still bf16
+    t = dense()
+    for n in ("q", "k", "v"):
+        t[n] = desc(t[n].shape[:4], _lib.ATTN_F16)
+    assert call_fwd(lib, t) == E["ATTN_E_DTYPE"]                 # out still bf16
     t = dense()
     t["dout"] = desc([2, 100, 4, 128], _lib.ATTN_F16)
     assert call_bwd(lib, t) == E["ATTN_E_DTYPE"]
+    t = dense()
+    t["dq"] = desc([2, 100, 4, 128], _lib.ATTN_F16)
+    assert call_bwd(lib, t) == E["ATTN_E_DTYPE"]
+    for bad in (_lib.ATTN_F32, _lib.ATTN_I32, _lib.ATTN_U8):
+        t = dense()
+        for n in ("q", "k", "v"):
+            t[n] = desc(t[n].shape[:4], bad)
+        assert call_fwd(lib, t) == E["ATTN_E_DTYPE"]
+
+
+def test_accepts_all_fp16(lib):
+    """All-fp16 tensors pass the element-type gate; the descriptors say host
+    memory (device -1), so the call stops at the device check and nothing is
+    launched even where a GPU is present."""
+    t = dense()
+    for n in t:
+        t[n] = desc(t[n].shape[:t[n].ndim],
+                    _lib.ATTN_F32 if n == "lse" else _lib.ATTN_F16, device=-1)
+    # ATTN_E_CUDA where no GPU is present (the device query itself fails)
+    stop = (E["ATTN_E_DEVICE"], E["ATTN_E_CUDA"])
+    assert call_fwd(lib, t) in stop
+    assert call_bwd(lib, t) in stop
 
 
 @pytest.mark.parametrize("D", [32, 96, 100, 112, 192, 256])
