@@ -89,7 +89,8 @@ __device__ __forceinline__ void stage_row_chunk(uint8_t* tile, int row, int col0
     }
 }
 
-template <int D, bool F16>
+// kMask: a user mask is present (its path is compiled only into that variant).
+template <int D, bool F16, bool kMask>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem p, const __grid_constant__ BwdMaps maps,
                                                   int with_dq) {
     using L = BwdLayout<D>;
@@ -326,7 +327,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             iter_tile(it, &h, &m0);
             const float* lse2 = vec + s * 256;
             const bool pred = (n0 + kT > si.len_k) || (m0 + kT > si.len_q) ||
-                              (p.causal && n0 + kT - 1 > m0) || (p.mask_kind != MASK_NONE);
+                              (p.causal && n0 + kT - 1 > m0) || kMask;
             // After a wait gives up, `ok` stays false: the warp skips the work
             // but still meets every named barrier, so none is left short.
             if (ok) {
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             }
             if (ok) {
                 tc_fence_after();
-                if (p.mask_kind != MASK_NONE) {
+                if constexpr (kMask) {
                     // With a user mask, rewrite this warp's chunks of S^T in TMEM as
                     // finished logits first (mask loads in the main loop would spill).
 #pragma unroll 1
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                     // address): loading all 32 up front costs 64 live registers.
                     const uint32_t va = smem_u32(lse2 + 32 * c);
                     uint32_t pk[16], dk[16];
-                    if (!pred && p.mask_kind == MASK_NONE) {
+                    if (!pred && !kMask) {
                         const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
                         float4 lv = lds128(va), dl = lds128(va + 512), lvn, dln;
 #pragma unroll
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                                 dl = dln;
                             }
                         }
-                    } else if (p.mask_kind == MASK_NONE) {
+                    } else if (!kMask) {
                         // keys past the sequence, query rows past it, causal pairs
                         const int qlo = p.causal ? j - m0 : -1;          // visible: q >= qlo
                         const int qhi = (j < si.len_k) ? si.len_q - m0 : 0;  // visible: q < qhi
@@ -542,7 +543,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
 
 // ------------------------------------------------------------------ host side
 
-template <int D, bool F16>
+template <int D, bool F16, bool kMask>
 cudaError_t launch_bwd_sm100_d(const Problem& p, bool with_dq, cudaStream_t stream) {
     using L = BwdLayout<D>;
     if (p.B == 0 || p.Sk == 0) return cudaSuccess;
@@ -567,22 +568,29 @@ cudaError_t launch_bwd_sm100_d(const Problem& p, bool with_dq, cudaStream_t stre
         maps.dq_acc = maps.k;   // never read without dQ
     }
     if (!ok) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(bwd_sm100_kernel<D, F16>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_sm100_kernel<D, F16, kMask>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((p.Sk + kT - 1) / kT, p.Hkv, p.B);
-    bwd_sm100_kernel<D, F16><<<grid, kBwdThreads, L::kBytes, stream>>>(p, maps, with_dq ? 1 : 0);
+    bwd_sm100_kernel<D, F16, kMask><<<grid, kBwdThreads, L::kBytes, stream>>>(p, maps, with_dq ? 1 : 0);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_main(const Problem& p, bool with_dq_atomics, cudaStream_t stream) {
-    if (p.f16)
-        return p.D == 64 ? launch_bwd_sm100_d<64, true>(p, with_dq_atomics, stream)
-                         : launch_bwd_sm100_d<128, true>(p, with_dq_atomics, stream);
-    return p.D == 64 ? launch_bwd_sm100_d<64, false>(p, with_dq_atomics, stream)
-                     : launch_bwd_sm100_d<128, false>(p, with_dq_atomics, stream);
+    const bool m = p.mask_kind != MASK_NONE;
+    const bool w = with_dq_atomics;
+    if (p.f16) {
+        if (m) return p.D == 64 ? launch_bwd_sm100_d<64, true, true>(p, w, stream)
+                                : launch_bwd_sm100_d<128, true, true>(p, w, stream);
+        return p.D == 64 ? launch_bwd_sm100_d<64, true, false>(p, w, stream)
+                         : launch_bwd_sm100_d<128, true, false>(p, w, stream);
+    }
+    if (m) return p.D == 64 ? launch_bwd_sm100_d<64, false, true>(p, w, stream)
+                            : launch_bwd_sm100_d<128, false, true>(p, w, stream);
+    return p.D == 64 ? launch_bwd_sm100_d<64, false, false>(p, w, stream)
+                     : launch_bwd_sm100_d<128, false, false>(p, w, stream);
 }
 
 }  // namespace attn
