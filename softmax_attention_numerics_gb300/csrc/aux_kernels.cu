@@ -11,48 +11,51 @@
 namespace attn {
 namespace {
 
-// One warp per (row, head); D/32 elements per lane.
+// D/8 threads per (row, head), 8 elements (16 bytes) of O and of dO per
+// thread: every load is a full 16-byte vector and a warp covers 32*8/D rows,
+// so the reduction is log2(D/8) shuffles within each row's lane group.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) preprocess_kernel(const Problem p, int64_t rows) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    constexpr int kTpr = D / 8;                       // threads per (row, head)
+    constexpr int kGpw = 32 / kTpr;                   // (row, head) groups per warp
+    const int sub = threadIdx.x & (kTpr - 1);         // position within the row
+    const int gw = (threadIdx.x & 31) / kTpr;         // group within the warp
+    const int64_t groups = static_cast<int64_t>(gridDim.x) * (blockDim.x / kTpr);
     const int64_t total = rows * p.Hq;
-    for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total;
-         w += nwarps) {
-        const int h = static_cast<int>(w % p.Hq);
-        const int64_t r = w / p.Hq;
-        int b;
-        int64_t i;
-        if (p.varlen) {
-            b = 0;
-            i = r;
-        } else {
-            b = static_cast<int>(r / p.Sq);
-            i = r - static_cast<int64_t>(b) * p.Sq;
-        }
-        const bf16* og = p.o + b * p.o_b + i * p.o_s + h * p.o_h;
-        const bf16* dg = p.dout + b * p.do_b + i * p.do_s + h * p.do_h;
+    // The loop bound is the warp's first group, so all 32 lanes run the same
+    // iterations and meet every shuffle; groups past the end idle.
+    for (int64_t w0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kGpw;
+         w0 < total; w0 += groups) {
+        const int64_t w = w0 + gw;
+        const bool active = w < total;
+        int b = 0, h = 0;
+        int64_t i = 0;
         float acc = 0.f;
-        if (D == 128) {
-            const uint2 ov = *reinterpret_cast<const uint2*>(og + lane * 4);
-            const uint2 dv = *reinterpret_cast<const uint2*>(dg + lane * 4);
-            const uint32_t ow[2] = {ov.x, ov.y}, dw[2] = {dv.x, dv.y};
+        if (active) {
+            h = static_cast<int>(w % p.Hq);
+            const int64_t r = w / p.Hq;
+            if (p.varlen) {
+                i = r;
+            } else {
+                b = static_cast<int>(r / p.Sq);
+                i = r - static_cast<int64_t>(b) * p.Sq;
+            }
+            const uint4 ov = *reinterpret_cast<const uint4*>(p.o + b * p.o_b + i * p.o_s +
+                                                             h * p.o_h + sub * 8);
+            const uint4 dv = *reinterpret_cast<const uint4*>(p.dout + b * p.do_b + i * p.do_s +
+                                                             h * p.do_h + sub * 8);
+            const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
+            for (int e = 0; e < 4; ++e) {
                 const float2 a = unpack2<F16>(ow[e]);
                 const float2 c = unpack2<F16>(dw[e]);
                 acc = fmaf(a.x, c.x, acc);
                 acc = fmaf(a.y, c.y, acc);
             }
-        } else {
-            const float2 a = unpack2<F16>(*reinterpret_cast<const uint32_t*>(og + lane * 2));
-            const float2 c = unpack2<F16>(*reinterpret_cast<const uint32_t*>(dg + lane * 2));
-            acc = fmaf(a.x, c.x, acc);
-            acc = fmaf(a.y, c.y, acc);
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
+        for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (active && sub == 0) {
             const int64_t li = b * p.lse_b + h * p.lse_h + i;
             p.delta[li] = acc;
             p.lse2[li] = p.lse[li] * kLog2e;
@@ -130,7 +133,7 @@ int grid_for(int64_t work, int threads) {
 cudaError_t launch_bwd_preprocess(const Problem& p, cudaStream_t stream) {
     const int64_t rows = p.varlen ? p.T : static_cast<int64_t>(p.B) * p.Sq;
     if (rows == 0) return cudaSuccess;
-    const int blocks = grid_for(rows * p.Hq * 32, 256);
+    const int blocks = grid_for(rows * p.Hq * (p.D / 8), 256);
     if (p.f16) {
         if (p.D == 64)
             preprocess_kernel<64, true><<<blocks, 256, 0, stream>>>(p, rows);

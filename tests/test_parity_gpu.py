@@ -159,6 +159,11 @@ EDGE = [
     (1, 260, 100, 2, 1, 64, True, "none"),           # Sq > Sk
     (1, 64, 0, 2, 1, 64, False, "none"),             # no keys at all
     (1, 0, 64, 2, 1, 128, False, "none"),            # no queries
+    (1, 1000, 1000, 16, 2, 128, True, "none"),       # GQA G=8: dK/dV summed over 8 q heads
+    (1, 1000, 1000, 16, 2, 64, False, "none"),
+    (4, 130, 130, 32, 32, 64, False, "none"),        # many small (batch, head) problems
+    (2, 257, 383, 8, 4, 128, False, "bool_rows"),    # ragged in both dimensions, per-row mask
+    (1, 513, 513, 4, 1, 128, True, "additive_random"),  # causal + additive mask, G=4
 ]
 
 
