@@ -44,6 +44,7 @@ def parse(argv=None):
     ap.add_argument("--seqlen", type=int, default=131072)
     ap.add_argument("--heads", type=int, default=16)
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128])
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
                     help="element type of q, k, v, dO and of the outputs")
     ap.add_argument("--deterministic", action="store_true",
@@ -60,8 +61,8 @@ def fwd_flops(B, H, S, D, causal):
 
 
 def workload_name(a):
-    return "long_seq B=1 H=%d S=%d D=128 %s%s fwd+bwd%s" % (
-        a.heads, a.seqlen, "causal" if a.causal else "non-causal",
+    return "long_seq B=1 H=%d S=%d D=%d %s%s fwd+bwd%s" % (
+        a.heads, a.seqlen, getattr(a, "head_dim", 128), "causal" if a.causal else "non-causal",
         " fp16" if getattr(a, "dtype", "bf16") == "f16" else "",
         " (deterministic dQ)" if a.deterministic else "")
 
@@ -78,7 +79,7 @@ def run_oracle_sample(a):
     against all S keys (full forward+backward arithmetic of those rows)."""
     import numpy as np
     from oracle import attn_oracle as O
-    S, D, m = a.seqlen, 128, a.cpu_oracle_sample
+    S, D, m = a.seqlen, a.head_dim, a.cpu_oracle_sample
     rng = np.random.default_rng(42)
     q = rng.standard_normal((m, D)).astype(np.float32).astype(np.float64)
     k = rng.standard_normal((S, D)).astype(np.float32).astype(np.float64)
@@ -106,7 +107,8 @@ def cpu_oracle(a, rows, reps):
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[var] = str(cores)
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-oracle-sample", str(rows),
-           "--cpu-oracle-reps", str(reps), "--seqlen", str(a.seqlen)]
+           "--cpu-oracle-reps", str(reps), "--seqlen", str(a.seqlen),
+           "--head-dim", str(a.head_dim)]
     if a.causal:
         cmd.append("--causal")
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
@@ -252,7 +254,7 @@ def run_reference(a):
         "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup, "ms_per_step": t * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": workload_name(a), "B": 1, "H": a.heads, "S": a.seqlen, "D": 128,
+        "config": {"workload": workload_name(a), "B": 1, "H": a.heads, "S": a.seqlen, "D": a.head_dim,
                    "causal": a.causal, "parallelism": "replicas" if a.gpus > 1 else "single",
                    "sample": "each step: fp64 oracle on query rows 0..%d of one head" % (rows - 1)},
         "cpu_baseline": cb,
@@ -296,7 +298,7 @@ def main():
         _build.build()
     lib = _lib.load()
 
-    B, H, S, D = 1, a.heads, a.seqlen, 128
+    B, H, S, D = 1, a.heads, a.seqlen, a.head_dim
     scale = 1.0 / math.sqrt(D)
     g = torch.Generator(device=dev).manual_seed(42 + rank)
     shape = (B, S, H, D)
