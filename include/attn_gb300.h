@@ -222,6 +222,18 @@ const char* attn_last_cuda_error(void);
 int attn_version(void);
 
 /*
+ * attn_selftest_wait_timeout - exercises the failure path of the bounded
+ * device waits on the current device: one thread waits on a device barrier
+ * that nothing will ever complete, gives up after `budget_us` microseconds
+ * (1 .. 1,000,000) of global time and sets the error word, so that a
+ * following attn_get_error(stream) returns ATTN_E_TIMEOUT.  The same wait
+ * loop bounds every wait in the attention kernels (there with a 2 s budget).
+ * Nothing hangs and the CUDA context stays usable.  Returns ATTN_OK once the
+ * probe is launched on `stream`, ATTN_E_ARG for a budget out of range.
+ */
+int attn_selftest_wait_timeout(uint32_t budget_us, attn_stream_t stream);
+
+/*
  * Profiling hooks (used by the benchmark; no effect on results).
  *
  * attn_profile_events - from now on, record the CUDA events `before` and

@@ -19,7 +19,7 @@ ERRORS = {
 # Every symbol the header declares.
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_bytes", "attn_get_error",
            "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_profile_events",
-           "attn_launch_count")
+           "attn_launch_count", "attn_selftest_wait_timeout")
 
 ATTN_STAGE_FWD, ATTN_STAGE_BWD_PREPROCESS, ATTN_STAGE_BWD_MAIN, ATTN_STAGE_BWD_DQ = 0, 1, 2, 3
 
@@ -79,6 +79,8 @@ def load():
     lib.attn_profile_events.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
     lib.attn_launch_count.restype = ctypes.c_ulonglong
     lib.attn_launch_count.argtypes = []
+    lib.attn_selftest_wait_timeout.restype = ctypes.c_int
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
     _lib = lib
     return lib
 

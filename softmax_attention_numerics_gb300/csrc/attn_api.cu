@@ -464,6 +464,18 @@ extern "C" const char* attn_strerror(int code) {
 
 extern "C" int attn_version(void) { return 100; }
 
+extern "C" int attn_selftest_wait_timeout(uint32_t budget_us, attn_stream_t stream) {
+    if (budget_us == 0 || budget_us > 1000000u) return ATTN_E_ARG;
+    int dev;
+    ATTN_TRY(current_device(&dev));
+    int* err = error_word(dev);
+    if (!err) return ATTN_E_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return run_stage(-1, st, [&] {
+        return launch_wait_timeout_probe(err, static_cast<uint64_t>(budget_us) * 1000ull, st);
+    });
+}
+
 extern "C" int attn_profile_events(int stage, void* before, void* after) {
     if (stage < 0 || stage >= ATTN_STAGE_COUNT) return ATTN_E_ARG;
     g_prof[stage][0] = static_cast<cudaEvent_t>(before);

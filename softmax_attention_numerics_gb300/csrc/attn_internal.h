@@ -87,5 +87,8 @@ cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_deterministic(const Problem& p, cudaStream_t stream);
 cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_zero_trailing_bwd(const Problem& p, cudaStream_t stream);
+// One CTA whose thread 0 waits, bounded by budget_ns, on an mbarrier that no
+// one arrives on, and then reports DEV_E_TIMEOUT through `err`.
+cudaError_t launch_wait_timeout_probe(int* err, uint64_t budget_ns, cudaStream_t stream);
 
 }  // namespace attn

@@ -7,6 +7,7 @@
 //                   PR #9, section 2; flash-dmattn PR #122, Root Cause 1).
 // All are grid-stride loops sized to a multiple of the SM count.
 #include "device_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace attn {
 namespace {
@@ -117,6 +118,24 @@ __global__ void zero_trailing_bwd_kernel(const Problem p) {
     zero_rows_bf16(p.dv, r0, p.T, p.Hkv, p.D);
 }
 
+// The bounded-wait path of the tcgen05 kernels, on its own: a wait that
+// nothing will satisfy gives up after budget_ns of global time and the error
+// word reports a timeout.  The barrier expects one arrival that never comes.
+__global__ void wait_timeout_probe_kernel(int* err, uint64_t budget_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        sm100::mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        sm100::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        volatile int* flag = &abort_flag;
+        if (!sm100::mbar_wait(smem_u32(&bar), 0, flag, budget_ns)) set_error(err, DEV_E_TIMEOUT);
+    }
+}
+
 int grid_for(int64_t work, int threads) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -156,6 +175,11 @@ cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream) {
         dq_convert_kernel<true><<<grid_for(n4, 256), 256, 0, stream>>>(p.dq_acc, p.dq, n4, p.scale);
     else
         dq_convert_kernel<false><<<grid_for(n4, 256), 256, 0, stream>>>(p.dq_acc, p.dq, n4, p.scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_probe(int* err, uint64_t budget_ns, cudaStream_t stream) {
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(err, budget_ns);
     return cudaGetLastError();
 }
 

@@ -69,7 +69,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // false if it gave up (abort flag set by someone else, or the budget ran
 // out, in which case this thread raises the flag).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag,
+                                          uint64_t budget_ns = kWaitBudgetNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     uint32_t n = 0;
@@ -77,7 +78,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
         if (mbar_try_wait(bar, parity)) return true;
         if ((++n & 63u) == 0) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > kWaitBudgetNs) {
+            if (global_ns() - t0 > budget_ns) {
                 *abort_flag = 1;
                 return false;
             }

@@ -241,3 +241,9 @@ def test_workspace_size_and_checks(lib):
     assert call_bwd(lib, t, ws=0, ws_bytes=n) == E["ATTN_E_WORKSPACE"]
     assert call_bwd(lib, t, ws=FAKE + 16, ws_bytes=n) == E["ATTN_E_WORKSPACE"]
     assert lib.attn_bwd_workspace_bytes(R(dense(D=96)["q"]), R(t["k"]), 0) == 0
+
+
+def test_selftest_wait_timeout_rejects_bad_budget(lib):
+    # checked before the device is touched
+    assert lib.attn_selftest_wait_timeout(0, None) == E["ATTN_E_ARG"]
+    assert lib.attn_selftest_wait_timeout(1000001, None) == E["ATTN_E_ARG"]
