@@ -281,10 +281,12 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
+    # Bind this rank's GPU before the process group so NCCL's communicator and
+    # every collective use it.
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
 
     # CPU baseline first: the oracle child process runs before this process
     # touches the GPU heavily (rank 0 at N=1 only).
