@@ -69,3 +69,26 @@ def test_reference_arm_runs_on_rank0_only(monkeypatch):
     with contextlib.redirect_stdout(buf):
         bench.run_reference(bench.parse(["--impl", "reference", "--gpus", "2"]))
     assert called == [] and buf.getvalue() == ""
+
+
+def test_reference_arm_json_contract():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON
+    line with the benchmark contract's keys, on a small workload."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--seqlen", "2048", "--heads", "2", "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["higher_is_better"] is True and d["steps"] == 1 and d["warmup"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["config"]["S"] == 2048 and d["config"]["H"] == 2
