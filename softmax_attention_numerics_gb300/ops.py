@@ -58,9 +58,10 @@ def attn_fwd(q, k, v, mask=None, cu_seqlens=None, max_seqlen=None, causal=False,
              out=None, lse=None, eager_rescale=False, stream=None):
     """Forward pass.  Returns (out, lse).
 
+    q, k, v: bf16 or fp16 (all the same); out has their type, lse is fp32.
     Dense: q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] -> out like q, lse [B,Hq,Sq] fp32.
     Varlen (cu_seqlens int32 [n+1]): q [T,Hq,D], k/v [T,Hkv,D], lse [Hq,T].
-    mask: bool (True = visible) or additive fp32/bf16, broadcastable to
+    mask: bool (True = visible) or additive fp32/bf16/fp16, broadcastable to
     [B,Hq,Sq,Sk].  scale=None means 1/sqrt(D).
     """
     lib = _lib.load()
