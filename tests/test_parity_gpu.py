@@ -274,6 +274,71 @@ def test_atomic_path_spread_within_fp32_reassociation_bound():
     assert np.all(spread <= bound + 1e-30)
 
 
+def test_atomic_spread_bound_holds_under_concurrent_load():
+    """The same reassociation bound with another stream keeping the GPU busy
+    (PFCCLab/cudnn-frontend PR #9: the spread criterion also under concurrent
+    load): the reduction order may change, the bound may not be exceeded."""
+    case = W.low_lse_row(392, 512, "bool", D=128)
+    ref = to64(gpu_run(case)["dq"])
+    side = torch.cuda.Stream()
+    a = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
+    runs = []
+    for _ in range(8):
+        with torch.cuda.stream(side):
+            for _ in range(4):
+                a = (a @ a).clamp_(-1, 1)           # busy work on another stream
+        runs.append(to64(gpu_run(case)["dq"]))
+    torch.cuda.synchronize()
+    runs = np.stack(runs + [ref])
+    spread = runs.max(0) - runs.min(0)
+    # the bound of the test above, computed the same way
+    q, k, v, do = (to64(case[n]) for n in ("q", "k", "v", "do"))
+    mask = oracle_mask(case["mask"])
+    sc = case["scale"]
+    sabs = np.zeros_like(q)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[2]):
+            bias = O.bias_for(mask, b, h, q.shape[1], k.shape[1], False)
+            P, _, _ = O._fwd_head(q[b, :, h], k[b, :, h], v[b, :, h], bias, sc)
+            dP = do[b, :, h] @ v[b, :, h].T
+            dS = P * (dP - (P * dP).sum(1)[:, None])
+            for t0 in range(0, k.shape[1], 128):
+                sabs[b, :, h] += np.abs(sc * dS[:, t0:t0 + 128] @ k[b, t0:t0 + 128, h])
+    n_terms = math.ceil(k.shape[1] / 128)
+    bound = 2 * (n_terms - 1) * 2.0 ** -24 * sabs + 2.0 ** -7 * np.abs(runs).max(0)
+    assert np.all(spread <= bound + 1e-30)
+
+
+def test_dq_strategy_leaves_other_outputs_bit_identical():
+    """Switching the dQ path (fp32 reductions vs the per-query-tile kernel)
+    changes only dq: out, lse, dk and dv come from the same kernels in the same
+    order and must be bit-identical (the "untouched outputs" check of
+    PFCCLab/cudnn-frontend PR #9)."""
+    for case in (W.low_lse_row(392, 512, "additive", D=64), W.varlen_gqa(n=4, hi=1024)):
+        a = gpu_run(case, deterministic=False)
+        b = gpu_run(case, deterministic=True)
+        for n in ("out", "lse", "dk", "dv"):
+            assert torch.equal(a[n], b[n]), n
+        assert_finite(a)
+        assert_finite(b)
+
+
+@pytest.mark.parametrize("mask", ["bool", "additive", "none"])
+@pytest.mark.parametrize("shape", [(392, 392), (100, 77)], ids=["392x392", "100x77"])
+def test_low_lse_row_bhsd_layout(shape, mask):
+    """The low-lse / partial-tile workload with BHSD buffers viewed as BSHD
+    (OpenWAM PR #64, Tests: the layout axis of the GPU matrix)."""
+    Sq, Sk = shape
+    case = W.low_lse_row(Sq, Sk, mask, D=128, row="last")
+    gcase = dict(case)
+    for n in ("q", "k", "v", "do"):
+        gcase[n] = case[n].transpose(1, 2).contiguous().cuda().transpose(1, 2)
+        assert not gcase[n].is_contiguous()
+    res = gpu_run(gcase)
+    assert_finite(res)
+    compare(res, oracle_dense(case), ctx="low_lse bhsd %s %s" % (shape, mask))
+
+
 # ------------------------------------------------------------- stream discipline
 
 def test_side_stream_with_busy_ambient_stream():
