@@ -222,10 +222,17 @@ def job_tflops(fwd_flop, steps, world, ms):
 
 
 def source_hash():
+    """Hash of the backward kernel's code (comments and blank lines removed, so
+    that a comment edit does not invalidate counters taken on the same code)."""
+    import re
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(l.rstrip() for l in text.splitlines() if l.strip())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

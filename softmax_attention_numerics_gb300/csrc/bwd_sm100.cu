@@ -21,8 +21,9 @@
 // and UMMA issuer; 10 = issues the dQ reductions and waits for them to read
 // the staging, so no compute warp ever blocks on the L2.
 // TMEM: dV | dK (D columns each) | S^T | dP^T (128 each).  Chunk c of S^T
-// (columns 32c .. 32c+31) is overwritten by its own packed bf16 P^T (first 16
-// columns) and dS^T (last 16) once read, so chunks never wait on each other;
+// (columns 32c .. 32c+31) is overwritten by its own packed 16-bit (bf16 or fp16,
+// the inputs' type) P^T (first 16 columns) and dS^T (last 16) once read, so
+// chunks never wait on each other;
 // dQ_i = dS K then takes dP^T's columns as one N = D accumulator.
 // dV / dK MMAs for chunks 0 and 2 run while chunks 1 and 3 are computed.
 //

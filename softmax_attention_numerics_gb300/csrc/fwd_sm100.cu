@@ -5,8 +5,9 @@
 //   warps 4-7   softmax for query tile 1
 //   warp  8     TMA producer: Q tiles once, then K_j, V_j through a ring
 //   warp  9     TMEM allocator and single-thread UMMA issuer
-// TMEM (512 columns): S0 | S1 (128 fp32 columns each; the bf16 P of a tile is
-// written over the first 64 columns of its S) | O0 | O1 (D columns each).
+// TMEM (512 columns): S0 | S1 (128 fp32 columns each; the 16-bit P of a tile,
+// bf16 or fp16 like the inputs, is written over the first 64 columns of its S)
+// | O0 | O1 (D columns each).
 //
 // Per key tile j the issuer runs, for t = 0, 1:
 //     O_t += P_t(j) V_j      (P from TMEM, V from shared memory)
@@ -22,7 +23,7 @@
 // exp2(m_ref - m_new) in TMEM; rows of the same warp that did not ask for a
 // rescale use a factor of exactly 1.  p = exp2(min(x - m_ref, 8)): the clamp
 // never fires on correct statistics (PFCCLab/cudnn-frontend PR #9, section 3).
-// Epilogue: out = O/lr (lr = sum of the bf16-rounded p that entered the MMA),
+// Epilogue: out = O/lr (lr = sum of the 16-bit-rounded p that entered the MMA),
 // lse = (m_ref + log2 l) ln 2 (l = sum of the exact p); l = 0 gives out = 0,
 // lse = 0.  Rows past the sequence are never stored (varlen neighbours).
 #include "sm100_ptx.cuh"
