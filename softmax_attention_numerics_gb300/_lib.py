@@ -1,6 +1,7 @@
 """ctypes view of the C ABI in include/attn_gb300.h (no torch types)."""
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -49,7 +50,25 @@ def load():
     global _lib
     if _lib is not None:
         return _lib
-    path = lib_path()
+    _lib = load_path(lib_path())
+    return _lib
+
+
+@contextlib.contextmanager
+def use_library(path):
+    """Route every call made inside the block through the library at `path`
+    (e.g. the poisoned-staging debug build), then restore the previous one."""
+    global _lib
+    prev = _lib
+    _lib = load_path(path)
+    try:
+        yield _lib
+    finally:
+        _lib = prev
+
+
+def load_path(path):
+    """Load and bind one build of the library."""
     if not os.path.exists(path):
         raise RuntimeError(
             "CUDA attention library not built (%s missing); run "
@@ -81,7 +100,6 @@ def load():
     lib.attn_launch_count.argtypes = []
     lib.attn_selftest_wait_timeout.restype = ctypes.c_int
     lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
-    _lib = lib
     return lib
 
 

@@ -46,15 +46,29 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
+# Debug variant: every shared-memory staging tile (dS for the dQ MMA, the fp32
+# dQ partial before its bulk reduction, the dK / dV epilogue tiles) is filled
+# with NaN by each writer just before its real data, so a consumer that reads
+# the tile before the writes have landed produces non-finite output.
+POISON_LIB = os.path.join(LIB_DIR, "libattn_gb300_poison.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant=None) -> str:
+    """variant None: the library; "poison": the poisoned-staging debug build."""
+    out_lib, build_dir = LIB, BUILD
+    if variant == "poison":
+        out_lib, build_dir = POISON_LIB, os.path.join(BUILD, "poison")
+        extra_flags = tuple(extra_flags) + ("-DATTN_POISON_SMEM",)
+    elif variant is not None:
+        raise ValueError("unknown build variant %r" % (variant,))
+    if variant is None and not force and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -66,13 +80,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = out_lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":

@@ -77,6 +77,18 @@ struct BwdMaps {
     CUtensorMap k, v, q, dout, dk, dv, dq_acc;
 };
 
+// Debug build (ATTN_POISON_SMEM): fill 16 staging bytes with NaN (all-ones is
+// NaN in fp32, bf16 and fp16) right before the real data, so that a consumer
+// that reads the tile before the writes land yields non-finite output.
+__device__ __forceinline__ void poison16(const void* p) {
+#ifdef ATTN_POISON_SMEM
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(smem_u32(p)), "r"(0xffffffffu)
+                 : "memory");
+#else
+    (void)p;
+#endif
+}
+
 // Write one 32-column chunk of a row into a TMA-layout staging tile
 // ([blocks][128 rows][128 B], 16-byte chunks XOR-swizzled by row mod 8).
 __device__ __forceinline__ void stage_row_chunk(uint8_t* tile, int row, int col0,
@@ -86,6 +98,7 @@ __device__ __forceinline__ void stage_row_chunk(uint8_t* tile, int row, int col0
     for (int v = 0; v < 4; ++v) {
         const int ch = ((col0 & 63) >> 3) + v;
         uint4* dst = reinterpret_cast<uint4*>(tile + blk * 16384 + row * 128 + ((ch ^ (row & 7)) << 4));
+        poison16(dst);
         *dst = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
     }
 }
@@ -465,10 +478,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
                         // chunks swizzled; even blocks in the query stage, odd in the dO stage.
                         uint8_t* base = smem + dq_stage_off(hq * (D / 64) + bb, s) + r * 128;
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
+                        for (int k = 0; k < 8; ++k) {
+                            poison16(base + ((k ^ (r & 7)) << 4));
                             *reinterpret_cast<uint4*>(base + ((k ^ (r & 7)) << 4)) =
                                 make_uint4(dq[32 * bb + 4 * k], dq[32 * bb + 4 * k + 1],
                                            dq[32 * bb + 4 * k + 2], dq[32 * bb + 4 * k + 3]);
+                        }
                     }
                 }
                 if (with_dq) fence_proxy_async_smem();   // each writer: its stores -> async proxy
