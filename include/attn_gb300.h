@@ -54,7 +54,9 @@
  *   Inputs q, k, v, dout, out (as a backward input): bf16 or fp16 (all the
  *   same type; it also sets the type of out, dq, dk, dv), last-dim stride 1,
  *   every other stride a multiple of 8 elements (16 bytes), base 16-byte
- *   aligned.  Outputs out, lse, dq, dk, dv: contiguous in the layouts above.
+ *   aligned.  Outputs out, lse, dq, dk, dv: contiguous in the layouts above,
+ *   base 16-byte aligned (lse keeps that contract as a backward input).  A
+ *   mask's base must be aligned to its element size, cu_seqlens to 4 bytes.
  *   Head dim D must be 64 or 128; Hq must be a multiple of Hkv (GQA).
  *   Causal masking is top-left aligned: key j is hidden from query i when
  *   j > i.  A query row with no visible key gets out = 0, lse = 0 and a zero
@@ -139,7 +141,8 @@ typedef struct {
  *               The mask is added after scaling.
  *   cu_seqlens  NULL for dense, else int32 [nseq+1] on the device (varlen).
  *   max_seqlen  varlen only: an upper bound on every sequence length (a
- *               longer sequence is skipped and flagged ATTN_E_SEQLENS).
+ *               longer sequence is skipped and flagged ATTN_E_SEQLENS; every
+ *               sequence is checked, also when max_seqlen is 0).
  *   causal      nonzero = causal (top-left).
  *   scale       finite softmax scale (callers usually pass 1/sqrt(D)).
  *   out         q's element type, same shape as q, contiguous; fully written.

@@ -161,6 +161,7 @@ int derive_shapes(const attn_tensor_t* q, const attn_tensor_t* k, const attn_ten
         if (cu->ndim != 1 || cu->shape[0] < 1) return ATTN_E_SHAPE;
         if (cu->stride[0] != 1 && cu->shape[0] > 1) return ATTN_E_LAYOUT;
         if (!cu->data) return ATTN_E_ARG;
+        if ((reinterpret_cast<uintptr_t>(cu->data) & 3u) != 0) return ATTN_E_LAYOUT;
         if (max_seqlen < 0) return ATTN_E_ARG;
         s->nseq = cu->shape[0] - 1;
         s->B = s->nseq;
@@ -277,6 +278,9 @@ int fill_common(Problem* p, const Shapes& s, const attn_tensor_t* q, const attn_
             p->mask_kind = MASK_F16;
         else
             return ATTN_E_DTYPE;
+        // the kernels load mask elements one by one: element alignment suffices
+        const uintptr_t esz = mask->dtype == ATTN_U8 ? 1 : (mask->dtype == ATTN_F32 ? 4 : 2);
+        if ((reinterpret_cast<uintptr_t>(mask->data) & (esz - 1)) != 0) return ATTN_E_LAYOUT;
         p->mask = mask->data;
         p->m_b = st[0];
         p->m_h = st[1];
@@ -386,9 +390,8 @@ extern "C" int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const at
     ATTN_TRY(check_input(dout, s.rank, s.elt));
     if (!same_shape(out, s.q_shape, s.rank) || !same_shape(dout, s.q_shape, s.rank))
         return ATTN_E_SHAPE;
-    if (lse->dtype != ATTN_F32) return ATTN_E_DTYPE;
-    if (!same_shape(lse, s.lse_shape, s.lse_rank)) return ATTN_E_SHAPE;
-    if (!is_contiguous(lse)) return ATTN_E_LAYOUT;
+    // lse is read back in the layout attn_fwd wrote it: the same contract as its output
+    ATTN_TRY(check_output(lse, ATTN_F32, s.lse_shape, s.lse_rank));
     ATTN_TRY(check_output(dq, s.elt, s.q_shape, s.rank));
     ATTN_TRY(check_output(dk, s.elt, s.k_shape, s.rank));
     ATTN_TRY(check_output(dv, s.elt, s.k_shape, s.rank));

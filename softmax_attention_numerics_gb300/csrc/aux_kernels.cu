@@ -2,7 +2,8 @@
 //   bwd_preprocess  Delta = rowsum(dO o O) in fp32 and lse2 = lse * log2(e)
 //   dq_convert      dq = bf16 / fp16 (dq_acc * scale)
 //   zero_trailing   rows >= cu[nseq] of a packed varlen buffer: out = 0 and
-//                   lse = 0 (forward), dq = dk = dv = 0 (backward).  Rows that no
+//                   lse = 0 (forward), dq = dk = dv = 0 (backward); also
+//                   checks every sequence's bounds against T and max_seqlen.  Rows that no
 //                   tile visits must still be written (PFCCLab/cudnn-frontend
 //                   PR #9, section 2; flash-dmattn PR #122, Root Cause 1).
 // All are grid-stride loops sized to a multiple of the SM count.
@@ -98,7 +99,20 @@ __device__ __forceinline__ void zero_rows_bf16(bf16* base, int64_t r0, int64_t T
         dst[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Every sequence's bounds, checked once per varlen call: the attention
+// kernels check only the sequences their blocks visit, and with max_seqlen = 0
+// no attention block runs at all.
+__device__ __forceinline__ void check_seqlens(const Problem& p) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < p.B;
+         b += stride) {
+        const int a = __ldg(p.cu + b), e = __ldg(p.cu + b + 1);
+        if (!(a >= 0 && e >= a && e <= p.T && e - a <= p.Sq)) set_error(p.err, DEV_E_SEQLENS);
+    }
+}
+
 __global__ void zero_trailing_fwd_kernel(const Problem p) {
+    check_seqlens(p);
     const int64_t r0 = trailing_start(p);
     zero_rows_bf16(p.out, r0, p.T, p.Hq, p.D);
     const int64_t n = (p.T - r0) * p.Hq;
@@ -112,6 +126,7 @@ __global__ void zero_trailing_fwd_kernel(const Problem p) {
 }
 
 __global__ void zero_trailing_bwd_kernel(const Problem p) {
+    check_seqlens(p);
     const int64_t r0 = trailing_start(p);
     zero_rows_bf16(p.dq, r0, p.T, p.Hq, p.D);
     zero_rows_bf16(p.dk, r0, p.T, p.Hkv, p.D);
@@ -184,14 +199,14 @@ cudaError_t launch_wait_timeout_probe(int* err, uint64_t budget_ns, cudaStream_t
 }
 
 cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream) {
-    if (!p.varlen || p.T == 0) return cudaSuccess;
+    if (!p.varlen || (p.T == 0 && p.B == 0)) return cudaSuccess;
     zero_trailing_fwd_kernel<<<grid_for(static_cast<int64_t>(p.T) * p.Hq * p.D / 8, 256), 256, 0,
                                stream>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_zero_trailing_bwd(const Problem& p, cudaStream_t stream) {
-    if (!p.varlen || p.T == 0) return cudaSuccess;
+    if (!p.varlen || (p.T == 0 && p.B == 0)) return cudaSuccess;
     zero_trailing_bwd_kernel<<<grid_for(static_cast<int64_t>(p.T) * p.Hq * p.D / 8, 256), 256,
                                0, stream>>>(p);
     return cudaGetLastError();

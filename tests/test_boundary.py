@@ -51,7 +51,10 @@ def test_version_and_strerror(lib):
         assert lib.attn_strerror(code)
 
 
-def desc(shape, dtype=_lib.ATTN_BF16, stride=None, data=FAKE, device=0):
+def desc(shape, dtype=_lib.ATTN_BF16, stride=None, data=FAKE, device=-1):
+    """Descriptor of a fake buffer.  The default device -1 (host memory) makes
+    a call that passes every host-side check stop at the device check, so no
+    call in this file can reach a launch, even where a GPU is present."""
     d = _lib.AttnTensor()
     d.data = data
     d.dtype = dtype
@@ -174,7 +177,7 @@ def test_strided_inputs_pass_validation(lib):
     t = dense()
     t["q"] = desc([2, 100, 4, 128], stride=[4 * 100 * 128, 128, 100 * 128, 1])
     rc = call_fwd(lib, t)
-    assert rc in (0, E["ATTN_E_CUDA"], E["ATTN_E_DEVICE"])
+    assert rc in (E["ATTN_E_CUDA"], E["ATTN_E_DEVICE"])
 
 
 def test_rejects_strided_out_params(lib):
@@ -200,6 +203,31 @@ def test_mask_contract(lib):
     assert call_fwd(lib, dense(), mask=three) == E["ATTN_E_SHAPE"]
 
 
+def test_rejects_misaligned_mask(lib):
+    # the kernels load mask elements one at a time: element alignment is the rule
+    stop = (E["ATTN_E_DEVICE"], E["ATTN_E_CUDA"])
+    for dtype, off, ok in ((_lib.ATTN_F32, 2, False), (_lib.ATTN_F32, 4, True),
+                           (_lib.ATTN_BF16, 1, False), (_lib.ATTN_F16, 1, False),
+                           (_lib.ATTN_BF16, 2, True), (_lib.ATTN_U8, 1, True)):
+        mask = desc([2, 1, 1, 77], dtype, data=FAKE + off)
+        rc = call_fwd(lib, dense(), mask=mask)
+        assert (rc in stop) if ok else rc == E["ATTN_E_LAYOUT"], (dtype, off)
+        rc = call_bwd(lib, dense(), mask=mask)
+        assert (rc in stop) if ok else rc == E["ATTN_E_LAYOUT"], (dtype, off)
+
+
+def test_bwd_lse_contract(lib):
+    t = dense()
+    t["lse"] = desc([2, 4, 100], _lib.ATTN_F32, data=0)
+    assert call_bwd(lib, t) == E["ATTN_E_ARG"]
+    t = dense()
+    t["lse"] = desc([2, 4, 100], _lib.ATTN_F32, data=FAKE + 4)
+    assert call_bwd(lib, t) == E["ATTN_E_LAYOUT"]
+    t = dense()
+    t["lse"] = desc([2, 4, 100], _lib.ATTN_F32, stride=[4 * 101, 101, 1])   # padded rows
+    assert call_bwd(lib, t) == E["ATTN_E_LAYOUT"]
+
+
 def varlen(T=1000, Hq=4, Hkv=2, D=64, n=3):
     return dict(q=desc([T, Hq, D]), k=desc([T, Hkv, D]), v=desc([T, Hkv, D]),
                 out=desc([T, Hq, D]), lse=desc([Hq, T], _lib.ATTN_F32), dout=desc([T, Hq, D]),
@@ -220,6 +248,10 @@ def test_varlen_contract(lib):
     t, cu = varlen()
     t["k"] = desc([999, 2, 64]); t["v"] = desc([999, 2, 64])
     assert call_fwd(lib, t, cu=cu, max_seqlen=512) == E["ATTN_E_SHAPE"]
+    t, cu = varlen()
+    cu.data = FAKE + 2                     # int32 offsets must be 4-byte aligned
+    assert call_fwd(lib, t, cu=cu, max_seqlen=512) == E["ATTN_E_LAYOUT"]
+    assert call_bwd(lib, t, cu=cu, max_seqlen=512) == E["ATTN_E_LAYOUT"]
 
 
 def test_host_pointers_rejected(lib):

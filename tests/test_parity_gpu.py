@@ -371,6 +371,28 @@ def test_malformed_cu_seqlens_sets_error_word():
     assert get_error() == 0
 
 
+def test_varlen_max_seqlen_zero_still_checks_sequences():
+    """With max_seqlen = 0 no attention block runs; a non-empty sequence must
+    still be reported (its rows would otherwise be left unwritten), and with
+    every sequence empty all rows are trailing rows: zero, no error."""
+    from softmax_attention_numerics_gb300 import attn_bwd, attn_fwd, get_error
+    T, H, D = 300, 2, 64
+    g = torch.Generator().manual_seed(3)
+    q, k, do = (torch.randn(T, H, D, generator=g).to(torch.bfloat16).cuda() for _ in range(3))
+    cu = torch.tensor([0, 100, 250], dtype=torch.int32, device="cuda")
+    assert get_error() == 0
+    out, lse = attn_fwd(q, k, k, cu_seqlens=cu, max_seqlen=0)
+    assert get_error() == -9
+    attn_bwd(q, k, k, q, do, torch.zeros(H, T, device="cuda"), cu_seqlens=cu, max_seqlen=0)
+    assert get_error() == -9
+    empty = torch.zeros(3, dtype=torch.int32, device="cuda")
+    out, lse = attn_fwd(q, k, k, cu_seqlens=empty, max_seqlen=0)
+    dq, dk, dv = attn_bwd(q, k, k, out, do, lse, cu_seqlens=empty, max_seqlen=0)
+    assert get_error() == 0
+    for x in (out, lse, dq, dk, dv):
+        assert not x.float().abs().gt(0).any()
+
+
 def test_cpu_tensors_rejected():
     from softmax_attention_numerics_gb300 import _lib, attn_fwd
     q = torch.randn(1, 8, 1, 64).to(torch.bfloat16)
