@@ -15,6 +15,7 @@ import pytest
 import torch
 
 from oracle import attn_oracle as O
+from parity_utils import oracle_mask
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 RNG = np.random.default_rng(1234)
@@ -400,6 +401,65 @@ def test_golden_overflow_threshold():
     with np.errstate(over="ignore"):
         assert np.isinf(np.exp(np.float32(-g["lse_threshold"] + 0.01)))
         assert np.isfinite(np.exp(np.float32(-g["lse_threshold"] - 0.01)))
+
+
+def _unpredicated_tile_dq_fp32(case, lse, delta, key_tile):
+    """dQ of the backward as OpenWAM PR #64 ("Summary") describes the broken
+    kernel, in fp32: the key axis is padded to a multiple of the key tile
+    with zero keys and zero values, and the padded columns of the last tile
+    see neither the mask nor any predicate (score 0, P = exp(0 - lse)).
+    The real columns use the oracle's statistics and are finite."""
+    q, k, v, do = (np.asarray(case[n].float().numpy(), np.float32) for n in ("q", "k", "v", "do"))
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    pad = (-Sk) % key_tile
+    scale = np.float32(case["scale"])
+    mask = oracle_mask(case["mask"])
+    dq = np.zeros_like(q)
+    with np.errstate(over="ignore", invalid="ignore"):
+        for b in range(B):
+            for h in range(H):
+                qh, kh, vh, doh = q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h]
+                s = scale * (qh @ kh.T)
+                if mask is not None:
+                    mb = np.broadcast_to(mask, (B, H, Sq, Sk))[b, h]
+                    s = np.where(mb, s, -np.inf) if mb.dtype == bool else s + mb.astype(np.float32)
+                kp = np.concatenate([kh, np.zeros((pad, D), np.float32)])
+                vp = np.concatenate([vh, np.zeros((pad, D), np.float32)])
+                sp = np.concatenate([s, np.zeros((Sq, pad), np.float32)], axis=1)   # unmasked zeros
+                P = np.exp(sp - lse[b, h][:, None].astype(np.float32))
+                dP = doh @ vp.T
+                dS = P * (dP - delta[b, h][:, None].astype(np.float32))
+                dq[b, :, h] = scale * (dS @ kp)
+    return dq
+
+
+def test_golden_openwam_partial_tile_counts():
+    """The page's table of non-finite dQ elements: the workload's anti-aligned
+    row has an lse below -ln(FLT_MAX), and computing the last partial key tile
+    without predicates turns exactly that row of dQ (B*H*D elements) non-finite
+    for each mask kind, nothing when the key count is a multiple of the tile,
+    and the oracle's own (predicated) gradients are finite everywhere."""
+    import attn_workloads as W
+    with open(os.path.join(GOLDEN, "openwam_partial_tile_nonfinite.json")) as f:
+        g = json.load(f)
+    for c in g["cases"]:
+        for kind, want in c["nonfinite_dq_unpredicated"].items():
+            case = W.low_lse_row(c["sq"], c["skv"], kind, D=g["D"], B=g["B"], H=g["H"])
+            q, k, v, do = (case[n].double().numpy() for n in ("q", "k", "v", "do"))
+            m = oracle_mask(case["mask"])
+            out, lse, dq, dk, dv = O.attn_bwd(q, k, v, do, mask=m, scale=case["scale"])
+            r = case["low_row"]
+            assert (lse[:, :, r] < g["lse_overflow_below"]).all()
+            others = np.delete(lse, r, axis=2)
+            assert (others > g["lse_overflow_below"]).all()
+            for x in (out, lse, dq, dk, dv):
+                assert np.isfinite(x).all()
+            delta = np.einsum("bshd,bshd->bhs", do, out)
+            bad = _unpredicated_tile_dq_fp32(case, lse, delta, g["key_tile"])
+            assert int((~np.isfinite(bad)).sum()) == want, (c, kind)
+            if want:                              # only the anti-aligned row
+                assert list(np.unique(np.nonzero(~np.isfinite(bad))[1])) == [r]
 
 
 # ---------------------------------------------------------------- mutation tests
