@@ -236,9 +236,17 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key):
+def traffic_workload(a):
+    """The workload key under which DRAM counters are stored."""
+    return "B=1 H=%d S=%d D=%d %s%s%s" % (
+        a.heads, a.seqlen, a.head_dim, "causal" if a.causal else "non-causal",
+        " fp16" if a.dtype == "f16" else "", " deterministic dQ" if a.deterministic else "")
+
+
+def ncu_traffic(kernel_key, workload):
     """Per-launch DRAM bytes from a committed ncu summary, or None when the
-    kernel source has changed since the counters were taken."""
+    counters were taken on another workload or the kernel source has changed
+    since they were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -246,7 +254,7 @@ def ncu_traffic(kernel_key):
     except (OSError, ValueError):
         return None
     e = d.get(kernel_key)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash() or e.get("workload") != workload:
         return None
     return e.get("bytes_per_launch_full")
 
@@ -382,7 +390,7 @@ def main():
     # main kernel: S, dP, dV, dK (+ dQ unless the per-query-tile kernel does it)
     main_flops = (2.0 if a.deterministic else 2.5) * ff
     main_achieved = main_flops / (stage_ms[_lib.ATTN_STAGE_BWD_MAIN] / 1e3) / 1e12
-    traffic = ncu_traffic("bwd_main")
+    traffic = ncu_traffic("bwd_main", traffic_workload(a))
     roofline = {"bound": "tensor", "kernel": "bwd_main", "achieved": main_achieved,
                 "peak": tensor_peak, "unit": "TFLOP/s", "frac": main_achieved / tensor_peak,
                 "traffic": traffic,

@@ -92,3 +92,22 @@ def test_reference_arm_json_contract():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["S"] == 2048 and d["config"]["H"] == 2
+
+
+def test_traffic_counters_only_for_the_captured_workload(monkeypatch):
+    """roofline.traffic comes from committed ncu counters: reported for the
+    workload and kernel code they were taken on, null for anything else."""
+    import json
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        stored = json.load(f)["bwd_main"]
+    monkeypatch.setattr(bench, "source_hash", lambda: stored["source_hash"])
+    default = bench.traffic_workload(bench.parse([]))
+    assert default == stored["workload"]
+    assert bench.ncu_traffic("bwd_main", default) == stored["bytes_per_launch_full"]
+    for flags in (["--causal"], ["--deterministic"], ["--dtype", "f16"], ["--head-dim", "64"],
+                  ["--seqlen", "65536"]):
+        w = bench.traffic_workload(bench.parse(flags))
+        assert w != default
+        assert bench.ncu_traffic("bwd_main", w) is None, flags
+    monkeypatch.setattr(bench, "source_hash", lambda: "0" * 16)
+    assert bench.ncu_traffic("bwd_main", default) is None
