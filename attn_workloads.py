@@ -24,6 +24,11 @@ Workloads (sizes and value distributions as the pages give them):
 * ``varlen_gqa``     16 packed sequences, lengths uniform in [128, 4096],
   Hq=32, Hkv=8, D=128, causal, 512 trailing rows that belong to no sequence.
 * ``long_seq``       B=1, H=16, D=128, S in {16384, 65536, 131072}.
+* ``fp8_qkv``        fp8 (E4M3) q, k, v with one descale factor per tensor:
+  q, k = N(0,1) with k scaled by 1000 / 5000 / 20000 and V = ones at
+  B=1, H=16, S=12288, D=128 (FlyDSL PR #1033, "The fp8 helper, second
+  commit"); each tensor is divided by amax/448 and rounded to E4M3 by
+  PyTorch's float8 conversion.
 """
 from __future__ import annotations
 
@@ -149,3 +154,23 @@ def sample_rows(B, H, S, n=64, seed=5):
             pick = sorted(set([0, S - 1] + idx))[:n]
             rows += [(b, h, i) for i in pick]
     return rows
+
+
+def _to_e4m3(x):
+    """fp32 tensor -> (E4M3 codes as uint8, descale) with descale = amax / 448."""
+    amax = float(x.abs().max()) if x.numel() else 0.0
+    d = amax / 448.0 if amax > 0 else 1.0
+    d = float(torch.tensor(d, dtype=torch.float32))          # an fp32 value
+    codes = (x / d).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, d
+
+
+def fp8_qkv(B=1, S=12288, H=16, D=128, k_scale=1000.0, v="ones", causal=False, seed=42):
+    """E4M3 codes q, k, v [B,S,H,D] (uint8) and their descale factors."""
+    g = _gen(seed)
+    q = _randn(g, (B, S, H, D))
+    k = _randn(g, (B, S, H, D)) * k_scale
+    vv = torch.ones(B, S, H, D) if v == "ones" else _randn(g, (B, S, H, D))
+    (qc, dq), (kc, dk), (vc, dv) = _to_e4m3(q), _to_e4m3(k), _to_e4m3(vv)
+    return dict(q=qc, k=kc, v=vc, descale_q=dq, descale_k=dk, descale_v=dv, causal=causal,
+                scale=1.0 / math.sqrt(D))

@@ -35,6 +35,10 @@ What it computes (the definition that every page relies on):
   gradients (PFCCLab/cudnn-frontend PR #9, section 2: rows the scheduler
   never visits must still be written).
 
+* fp8 inputs: E4M3 codes with one descale factor per tensor are decoded
+  from the format's definition and the forward is the same definition on
+  the decoded values (FlyDSL PR #1033, "The fp8 helper, second commit").
+
 Layouts follow the library: q/out/dout [B, Sq, Hq, D]; k/v [B, Sk, Hkv, D];
 lse [B, Hq, Sq]; varlen q [T, Hq, D], k/v [T, Hkv, D], lse [Hq, T].
 Masks are broadcastable to [B, Hq, Sq, Sk]: a bool array (True = visible) or a
@@ -48,6 +52,8 @@ import numpy as np
 
 __all__ = [
     "attn_fwd",
+    "attn_fwd_fp8",
+    "e4m3_decode",
     "attn_bwd",
     "attn_varlen",
     "attn_rows",
@@ -239,3 +245,34 @@ def attn_rows(q, k, v, dout, rows, mask=None, causal=False, scale=None):
         lses[idxs] = l
         dqs[idxs] = gq
     return outs, lses, dqs
+
+
+# ---------------------------------------------------------------- fp8 inputs
+
+def e4m3_decode(codes):
+    """Value of each 8-bit E4M3 code (the OCP 8-bit floating-point format's
+    finite-only E4M3: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+    bits; exponent field 0 encodes subnormals m/8 * 2^-6; S.1111.111 is NaN
+    and there is no infinity, so the largest finite magnitude is
+    1.75 * 2^8 = 448)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+def attn_fwd_fp8(q_codes, k_codes, v_codes, descale_q, descale_k, descale_v, causal=False,
+                 scale=None):
+    """Forward on fp8 inputs: q, k, v are E4M3 codes with one descale factor
+    per tensor (real value = decoded code * descale).  The fp8 forward of
+    FlyDSL PR #1033 ("The fp8 helper, second commit") still computes
+    softmax(scale * q k^T) v; only its route there (P rounded to fp8 for the
+    P V product, a lazily rebased running max) is fp8-specific, so the oracle
+    is the fp64 definition on the decoded inputs."""
+    q = e4m3_decode(q_codes) * float(descale_q)
+    k = e4m3_decode(k_codes) * float(descale_k)
+    v = e4m3_decode(v_codes) * float(descale_v)
+    return attn_fwd(q, k, v, causal=causal, scale=scale)

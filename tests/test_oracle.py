@@ -462,6 +462,62 @@ def test_golden_openwam_partial_tile_counts():
                 assert list(np.unique(np.nonzero(~np.isfinite(bad))[1])) == [r]
 
 
+# ---------------------------------------------------------------- fp8 inputs
+
+def test_e4m3_decode_matches_torch_on_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = O.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert list(np.nonzero(np.isnan(mine))[0]) == [0x7F, 0xFF]
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+
+
+def test_e4m3_decode_worked_values():
+    # straight from the format: bias 7, 3 mantissa bits, subnormals m/8 * 2^-6
+    table = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+             0x38: 1.0, 0x3C: 1.5, 0x40: 2.0, 0x77: 240.0, 0x7E: 448.0,
+             0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+    got = O.e4m3_decode(np.array(list(table), dtype=np.uint8))
+    assert list(got) == list(table.values())
+
+
+def test_fp8_generator_maps_each_amax_to_448():
+    import attn_workloads as W
+    c = W.fp8_qkv(S=512, H=2, D=64, k_scale=5000.0, v="randn")
+    for n in ("q", "k", "v"):
+        x = O.e4m3_decode(c[n].numpy())
+        assert np.isfinite(x).all()
+        assert np.abs(x).max() == 448.0
+
+
+def test_fp8_forward_with_unit_values_returns_the_value():
+    """Softmax weights sum to one, so with V = ones (one E4M3 code, 448 after
+    the amax scaling) every output is 448 * descale_v, at any logit spread."""
+    import attn_workloads as W
+    for ks in (1.0, 1000.0, 20000.0):
+        c = W.fp8_qkv(S=384, H=2, D=128, k_scale=ks, v="ones")
+        out, lse = O.attn_fwd_fp8(c["q"].numpy(), c["k"].numpy(), c["v"].numpy(), c["descale_q"],
+                                  c["descale_k"], c["descale_v"], scale=c["scale"])
+        assert np.all(np.abs(out - 448.0 * c["descale_v"]) < 1e-12)
+        assert np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_matches_torch_sdpa_on_decoded_inputs(causal):
+    import attn_workloads as W
+    c = W.fp8_qkv(B=2, S=200, H=2, D=64, k_scale=8.0, v="randn", causal=causal)
+    dec = {n: torch.from_numpy(c[n].numpy()).view(torch.float8_e4m3fn).to(torch.float64)
+              * c["descale_" + n] for n in ("q", "k", "v")}
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        dec["q"].transpose(1, 2), dec["k"].transpose(1, 2), dec["v"].transpose(1, 2),
+        is_causal=causal, scale=c["scale"]).transpose(1, 2).numpy()
+    out, _ = O.attn_fwd_fp8(c["q"].numpy(), c["k"].numpy(), c["v"].numpy(), c["descale_q"],
+                            c["descale_k"], c["descale_v"], causal=causal, scale=c["scale"])
+    assert np.abs(out - ref).max() < 1e-10
+
+
 # ---------------------------------------------------------------- mutation tests
 
 ORIG_BWD = O._bwd_head
