@@ -279,3 +279,16 @@ def test_selftest_wait_timeout_rejects_bad_budget(lib):
     # checked before the device is touched
     assert lib.attn_selftest_wait_timeout(0, None) == E["ATTN_E_ARG"]
     assert lib.attn_selftest_wait_timeout(1000001, None) == E["ATTN_E_ARG"]
+
+
+def test_poisoned_staging_variant_builds_and_exports_the_abi():
+    """The race-check debug library (ATTN_POISON_SMEM) compiles for sm_103a
+    from the same sources and exports the same C ABI."""
+    path = build.build(variant="poison")
+    assert path == build.POISON_LIB and os.path.exists(path)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True,
+                         text=True).stdout
+    for name in declared_functions():
+        assert re.search(r"\bT %s\b" % name, out), name
+    with pytest.raises(ValueError):
+        build.build(variant="nonexistent")
