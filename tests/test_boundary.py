@@ -292,3 +292,22 @@ def test_poisoned_staging_variant_builds_and_exports_the_abi():
         assert re.search(r"\bT %s\b" % name, out), name
     with pytest.raises(ValueError):
         build.build(variant="nonexistent")
+
+
+def test_use_library_swaps_and_restores(lib):
+    """Calls inside `use_library` go through the named build; the previous
+    library comes back afterwards, also when the block raises."""
+    path = build.build(variant="poison")
+    before = _lib.load()
+    with _lib.use_library(path) as dbg:
+        assert _lib.load() is dbg and dbg is not before
+        assert dbg.attn_version() == before.attn_version()
+    assert _lib.load() is before
+    with pytest.raises(RuntimeError):
+        with _lib.use_library(path):
+            raise RuntimeError("inside")
+    assert _lib.load() is before
+    with pytest.raises(RuntimeError, match="not built"):
+        with _lib.use_library(os.path.join(build.LIB_DIR, "missing.so")):
+            pass
+    assert _lib.load() is before
