@@ -39,10 +39,10 @@ def _deps():
         os.path.join(ROOT, "include", "attn_gb300.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
@@ -61,8 +61,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), variant=No
         extra_flags = tuple(extra_flags) + ("-DATTN_POISON_SMEM",)
     elif variant is not None:
         raise ValueError("unknown build variant %r" % (variant,))
-    if variant is None and not force and up_to_date():
-        return LIB
+    if not force and up_to_date(out_lib):
+        return out_lib
     os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     cc = nvcc()
