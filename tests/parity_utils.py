@@ -72,7 +72,7 @@ def compare(got, ref, names=("out", "lse", "dq", "dk", "dv"), ctx=""):
     for n in names:
         g = to64(got[n]) if torch.is_tensor(got[n]) else got[n]
         r = ref[n]
-        # the reference itself must be finite before it can judge anything
+        # the reference itself must be finite before it can serve as one
         # (FlyDSL PR #1033, review: NaN and Inf reported on both sides)
         assert np.isfinite(r).all(), "%s: oracle %s not finite" % (ctx, n)
         if n == "lse":

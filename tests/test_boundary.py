@@ -320,3 +320,16 @@ def test_fp8_forward_contract(lib):
     assert n == -(-2 * 2 * 128 * 208 // 256) * 256                  # keys padded to 208
     assert call_fwd_fp8(lib, fp8_dense(), ws_bytes=n - 1) == E["ATTN_E_WORKSPACE"]
     assert call_fwd_fp8(lib, fp8_dense(), ws=FAKE + 16, ws_bytes=n) == E["ATTN_E_WORKSPACE"]
+
+
+def test_poisoned_staging_variant_builds_and_exports_the_abi():
+    """The race-check debug library (ATTN_POISON_SMEM) compiles for sm_103a
+    from the same sources and exports the same C ABI."""
+    path = build.build(variant="poison")
+    assert path == build.POISON_LIB and os.path.exists(path)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True,
+                         text=True).stdout
+    for name in declared_functions():
+        assert re.search(r"\bT %s\b" % name, out), name
+    with pytest.raises(ValueError):
+        build.build(variant="nonexistent")
