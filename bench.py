@@ -45,8 +45,9 @@ def parse(argv=None):
     ap.add_argument("--heads", type=int, default=16)
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128])
-    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
-                    help="element type of q, k, v, dO and of the outputs")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16", "e4m3"],
+                    help="element type of q, k, v, dO and of the outputs; e4m3: the fp8 "
+                         "forward alone (bf16 out)")
     ap.add_argument("--deterministic", action="store_true",
                     help="dQ by the per-query-tile kernel instead of fp32 reductions")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -240,7 +241,7 @@ def traffic_workload(a):
     """The workload key under which DRAM counters are stored."""
     return "B=1 H=%d S=%d D=%d %s%s%s" % (
         a.heads, a.seqlen, a.head_dim, "causal" if a.causal else "non-causal",
-        " fp16" if a.dtype == "f16" else "", " deterministic dQ" if a.deterministic else "")
+        {"f16": " fp16", "e4m3": " fp8"}.get(a.dtype, ""), " deterministic dQ" if a.deterministic else "")
 
 
 def ncu_traffic(kernel_key, workload):
@@ -287,6 +288,107 @@ def run_reference(a):
     print(json.dumps(line))
 
 
+# ---------------------------------------------------------------- fp8 forward
+
+def run_fp8_forward(a):
+    """--dtype e4m3: the fp8 forward alone.  One step = the V transpose and the
+    forward kernel; metric fwd TFLOP/s against the fp8 peak, taken as twice
+    the measured bf16 peak (the nominal dense ratio 4.5 / 2.25 PFLOP/s)."""
+    import torch
+    from softmax_attention_numerics_gb300 import _lib, attn_fwd_fp8, fwd_fp8_workspace_bytes
+    from softmax_attention_numerics_gb300 import build as _build
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    lib = _lib.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B, H, S, D = 1, a.heads, a.seqlen, 128
+    g = torch.Generator(device=dev).manual_seed(42)
+
+    def fp8(x):
+        d = float(x.abs().max()) / 448.0
+        return (x / d).to(torch.float8_e4m3fn), d
+
+    (q, dq_), (k, dk_), (v, dv_) = (fp8(torch.randn(B, S, H, D, generator=g, device=dev))
+                                    for _ in range(3))
+    out = torch.empty(B, S, H, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+    ws = torch.empty(fwd_fp8_workspace_bytes(k), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        attn_fwd_fp8(q, k, v, dq_, dk_, dv_, causal=a.causal, out=out, lse=lse, workspace=ws,
+                     stream=stream)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(a.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            step()
+    stream.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = lib.attn_launch_count()
+    with ClockSampler(0) as clk:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(a.steps):
+                lib.attn_profile_events(_lib.ATTN_STAGE_FWD, ctypes_ptr(ev[i][0]), ctypes_ptr(ev[i][1]))
+                step()
+            t1.record(stream)
+        lib.attn_profile_events(_lib.ATTN_STAGE_FWD, None, None)
+        stream.synchronize()
+    launches = lib.attn_launch_count() - launches0
+    ms = t0.elapsed_time(t1)
+    ff = fwd_flops(B, H, S, D, a.causal)
+    value = ff * a.steps / (ms / 1e3) / 1e12
+    kern_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    achieved = ff / (kern_ms / 1e3) / 1e12
+    peaks, kind = measured_peaks()
+    peak = 2.0 * peaks.get("bf16_tflops_sustained", 1700.0)
+    nonfinite = sum(int((~torch.isfinite(t.float())).sum()) for t in (out, lse))
+
+    # e2e: host fp8 inputs in, out and lse back, copies inside the timed region
+    host_in = [t.view(torch.uint8).cpu().pin_memory() for t in (q, k, v)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out, lse)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e_steps = max(1, min(a.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream), ClockSampler(0) as e_clk:
+        e0.record(stream)
+        for _ in range(e_steps):
+            for dst, src in zip((q, k, v), host_in):
+                dst.view(torch.uint8).copy_(src, non_blocking=True)
+            step()
+            for dst, src in zip(host_out, (out, lse)):
+                dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    line = {
+        "metric": "attention fwd TFLOP/s, fp8 E4M3 inputs (bf16 out)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": "long_seq B=1 H=%d S=%d D=128 %s fwd fp8" % (
+                       H, S, "causal" if a.causal else "non-causal"),
+                   "B": B, "H": H, "S": S, "D": D, "causal": a.causal, "parallelism": "single",
+                   "l2": "no flush: every input tensor (%d MiB) exceeds L2" % (q.numel() >> 20)},
+        "roofline": {"bound": "tensor", "kernel": "fwd_fp8", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": "2 x %s bf16_tflops_sustained" % kind},
+        "cpu_baseline": None,
+        "e2e": {"value": ff * e_steps / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+                "clocks": e_clk.summary()},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "extra": {"fwd_kernel_ms": kern_ms, "nonfinite_outputs": nonfinite},
+    }
+    print(json.dumps(line))
+
+
 # ---------------------------------------------------------------- our arm
 
 def main():
@@ -296,6 +398,11 @@ def main():
         return
     if a.impl == "reference":
         run_reference(a)
+        return
+    if a.dtype == "e4m3":
+        if a.head_dim != 128 or a.deterministic or int(os.environ.get("WORLD_SIZE", "1")) > 1:
+            raise SystemExit("--dtype e4m3: one GPU, D = 128, forward only")
+        run_fp8_forward(a)
         return
 
     import torch

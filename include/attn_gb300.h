@@ -90,7 +90,8 @@ enum {
     ATTN_F16 = 2,   /* IEEE half: computed like bf16 (fp32 accumulation) */
     ATTN_F32 = 3,
     ATTN_I32 = 4,
-    ATTN_U8 = 5     /* bool mask: nonzero = visible, 0 = hidden */
+    ATTN_U8 = 5,    /* bool mask: nonzero = visible, 0 = hidden */
+    ATTN_E4M3 = 6   /* fp8 E4M3 (finite-only, max 448): attn_fwd_fp8 inputs */
 };
 
 /* Return codes. */
@@ -121,7 +122,7 @@ enum {
 
 typedef struct {
     void* data;          /* device pointer */
-    int32_t dtype;       /* ATTN_BF16, ATTN_F16, ATTN_F32, ATTN_I32, ATTN_U8 */
+    int32_t dtype;       /* ATTN_BF16, ATTN_F16, ATTN_F32, ATTN_I32, ATTN_U8, ATTN_E4M3 */
     int32_t ndim;        /* 1 .. 4 */
     int64_t shape[4];
     int64_t stride[4];   /* in elements; 0 = broadcast (masks only) */
@@ -155,6 +156,34 @@ int attn_fwd(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t
              const attn_tensor_t* mask, const attn_tensor_t* cu_seqlens, int32_t max_seqlen,
              int causal, float scale, attn_tensor_t* out, attn_tensor_t* lse,
              uint32_t flags, attn_stream_t stream);
+
+/*
+ * attn_fwd_fp8 - forward pass on fp8 inputs: out (bf16) and lse.
+ *
+ * Follows FlyDSL PR #1033 ("The fp8 helper, second commit"): the logits come
+ * from fp8 operands and the probabilities enter the P.V product as fp8; the
+ * result is still softmax(scale * q k^T) v of the real-valued inputs.
+ *
+ *   q, k, v     ATTN_E4M3 codes, dense [B,Sq,Hq,D] / [B,Sk,Hkv,D], D = 128;
+ *               last-dim stride 1, other strides multiples of 16 elements,
+ *               16-byte aligned bases.  Real value = decoded code * descale.
+ *   descale_q, descale_k, descale_v   finite, > 0 (one per tensor).
+ *   causal      nonzero = causal (top-left).  No mask, no varlen.
+ *   scale       finite softmax scale applied to the real-valued q . k.
+ *   out         ATTN_BF16 [B,Sq,Hq,D], contiguous; fully written.
+ *   lse         fp32 [B,Hq,Sq], contiguous; natural log; fully written.
+ *   workspace   device buffer of attn_fwd_fp8_workspace_bytes(k) bytes,
+ *               256-byte aligned (holds V transposed to [B,Hkv,D,Sk']).
+ *   flags       0 or ATTN_EAGER_RESCALE.
+ */
+int attn_fwd_fp8(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t* v,
+                 float descale_q, float descale_k, float descale_v, int causal, float scale,
+                 attn_tensor_t* out, attn_tensor_t* lse, void* workspace,
+                 size_t workspace_bytes, uint32_t flags, attn_stream_t stream);
+
+/* attn_fwd_fp8_workspace_bytes - workspace size attn_fwd_fp8 needs for k's
+ * shape (0 if k is malformed). */
+size_t attn_fwd_fp8_workspace_bytes(const attn_tensor_t* k);
 
 /*
  * attn_bwd_workspace_bytes - size of the scratch buffer attn_bwd needs for

@@ -7,7 +7,7 @@ import os
 
 from . import build as _build
 
-ATTN_BF16, ATTN_F16, ATTN_F32, ATTN_I32, ATTN_U8 = 1, 2, 3, 4, 5
+ATTN_BF16, ATTN_F16, ATTN_F32, ATTN_I32, ATTN_U8, ATTN_E4M3 = 1, 2, 3, 4, 5, 6
 ATTN_DETERMINISTIC = 1
 ATTN_EAGER_RESCALE = 2
 
@@ -18,7 +18,7 @@ ERRORS = {
 }
 
 # Every symbol the header declares.
-EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_bytes", "attn_get_error",
+EXPORTS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_fp8_workspace_bytes", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_bytes", "attn_get_error",
            "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_profile_events",
            "attn_launch_count", "attn_selftest_wait_timeout")
 
@@ -77,6 +77,12 @@ def load_path(path):
     lib.attn_fwd.restype = ctypes.c_int
     lib.attn_fwd.argtypes = [PT, PT, PT, PT, PT, ctypes.c_int32, ctypes.c_int, ctypes.c_float,
                              PT, PT, ctypes.c_uint32, ctypes.c_void_p]
+    lib.attn_fwd_fp8.restype = ctypes.c_int
+    lib.attn_fwd_fp8.argtypes = [PT, PT, PT, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                 ctypes.c_int, ctypes.c_float, PT, PT, ctypes.c_void_p,
+                                 ctypes.c_size_t, ctypes.c_uint32, ctypes.c_void_p]
+    lib.attn_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_fwd_fp8_workspace_bytes.argtypes = [PT]
     lib.attn_bwd.restype = ctypes.c_int
     lib.attn_bwd.argtypes = [PT, PT, PT, PT, PT, PT, PT, PT, ctypes.c_int32, ctypes.c_int,
                              ctypes.c_float, PT, PT, PT, ctypes.c_void_p, ctypes.c_size_t,

@@ -352,6 +352,103 @@ extern "C" int attn_fwd(const attn_tensor_t* q, const attn_tensor_t* k, const at
     return run_stage(ATTN_STAGE_FWD, st, [&] { return launch_fwd(p, st); });
 }
 
+namespace attn {
+namespace {
+
+// E4M3 input of the fp8 forward: rank 4, last stride 1, other strides multiples
+// of 16 elements (bytes) for dims longer than 1, 16-byte aligned base.
+int check_fp8_input(const attn_tensor_t* t) {
+    if (!t) return ATTN_E_ARG;
+    if (t->dtype != ATTN_E4M3) return ATTN_E_DTYPE;
+    if (t->ndim != 4) return ATTN_E_SHAPE;
+    int64_t n = 1;
+    for (int i = 0; i < 4; ++i) {
+        if (t->shape[i] < 0) return ATTN_E_SHAPE;
+        n *= t->shape[i];
+    }
+    if (n > 0 && !t->data) return ATTN_E_ARG;
+    if (t->stride[3] != 1) return ATTN_E_LAYOUT;
+    for (int i = 0; i < 3; ++i)
+        if (t->shape[i] > 1 && (t->stride[i] <= 0 || (t->stride[i] % 16) != 0)) return ATTN_E_LAYOUT;
+    if (!aligned16(t->data)) return ATTN_E_LAYOUT;
+    return ATTN_OK;
+}
+
+int64_t fp8_keys_padded(int64_t Sk) { return (Sk + 15) / 16 * 16; }
+
+size_t fp8_workspace(const attn_tensor_t* k) {
+    if (!k || k->ndim != 4 || k->shape[3] != 128) return 0;
+    for (int i = 0; i < 4; ++i)
+        if (k->shape[i] < 0) return 0;
+    return round256(static_cast<size_t>(k->shape[0] * k->shape[2] * 128 * fp8_keys_padded(k->shape[1])));
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" size_t attn_fwd_fp8_workspace_bytes(const attn_tensor_t* k) { return fp8_workspace(k); }
+
+extern "C" int attn_fwd_fp8(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t* v,
+                            float descale_q, float descale_k, float descale_v, int causal,
+                            float scale, attn_tensor_t* out, attn_tensor_t* lse, void* workspace,
+                            size_t workspace_bytes, uint32_t flags, attn_stream_t stream) {
+    if (!q || !k || !v) return ATTN_E_ARG;
+    if (q->dtype != ATTN_E4M3 || k->dtype != ATTN_E4M3 || v->dtype != ATTN_E4M3) return ATTN_E_DTYPE;
+    if (q->ndim == 4 && q->shape[3] != 128) return ATTN_E_UNSUPPORTED;
+    ATTN_TRY(check_fp8_input(q));
+    ATTN_TRY(check_fp8_input(k));
+    ATTN_TRY(check_fp8_input(v));
+    const int64_t B = q->shape[0], Sq = q->shape[1], Hq = q->shape[2], D = q->shape[3];
+    const int64_t Sk = k->shape[1], Hkv = k->shape[2];
+    if (k->shape[0] != B || k->shape[3] != D || !same_shape(v, k->shape, 4)) return ATTN_E_SHAPE;
+    if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return ATTN_E_SHAPE;
+    if (Sq > INT32_MAX / 2 || Sk > INT32_MAX / 2 || B > 65535 || Hq > 65535) return ATTN_E_UNSUPPORTED;
+    const int64_t qshape[4] = {B, Sq, Hq, D};
+    const int64_t lshape[3] = {B, Hq, Sq};
+    ATTN_TRY(check_output(out, ATTN_BF16, qshape, 4));
+    ATTN_TRY(check_output(lse, ATTN_F32, lshape, 3));
+    if (!isfinite(scale) || !isfinite(descale_q) || !isfinite(descale_k) || !isfinite(descale_v) ||
+        !(descale_q > 0.f) || !(descale_k > 0.f) || !(descale_v > 0.f))
+        return ATTN_E_ARG;
+    const size_t need = fp8_workspace(k);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return ATTN_E_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_E_WORKSPACE;
+    }
+    Fp8Problem p = {};
+    p.q = static_cast<const uint8_t*>(q->data);
+    p.k = static_cast<const uint8_t*>(k->data);
+    p.v = static_cast<const uint8_t*>(v->data);
+    p.vt = static_cast<uint8_t*>(workspace);
+    p.q_b = q->stride[0]; p.q_s = q->stride[1]; p.q_h = q->stride[2];
+    p.k_b = k->stride[0]; p.k_s = k->stride[1]; p.k_h = k->stride[2];
+    p.v_b = v->stride[0]; p.v_s = v->stride[1]; p.v_h = v->stride[2];
+    p.Sk_pad = static_cast<int>(fp8_keys_padded(Sk));
+    p.vt_h = static_cast<int64_t>(128) * p.Sk_pad;
+    p.vt_b = p.vt_h * Hkv;
+    p.out = static_cast<bf16*>(out->data);
+    p.lse = static_cast<float*>(lse->data);
+    p.out_b = Sq * Hq * D; p.out_s = Hq * D; p.out_h = D;
+    p.lse_b = Hq * Sq; p.lse_h = Sq;
+    p.B = static_cast<int>(B); p.Hq = static_cast<int>(Hq); p.Hkv = static_cast<int>(Hkv);
+    p.G = static_cast<int>(Hq / Hkv);
+    p.Sq = static_cast<int>(Sq); p.Sk = static_cast<int>(Sk);
+    p.causal = causal ? 1 : 0;
+    p.lazy = (flags & ATTN_EAGER_RESCALE) ? 0 : 1;
+    p.scale_log2 = scale * descale_q * descale_k * 1.4426950408889634f;
+    p.out_scale = descale_v;
+    int dev;
+    ATTN_TRY(current_device(&dev));
+    for (const attn_tensor_t* t : {q, k, v, static_cast<const attn_tensor_t*>(out),
+                                   static_cast<const attn_tensor_t*>(lse)})
+        ATTN_TRY(check_device(t, dev));
+    p.err = error_word(dev);
+    if (!p.err) return ATTN_E_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    ATTN_TRY(run_stage(-1, st, [&] { return launch_fp8_transpose_v(p, st); }));
+    return run_stage(ATTN_STAGE_FWD, st, [&] { return launch_fwd_fp8(p, st); });
+}
+
 extern "C" size_t attn_bwd_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* k,
                                            uint32_t flags) {
     if (!q || !k) return 0;
@@ -457,7 +554,7 @@ extern "C" const char* attn_strerror(int code) {
         case ATTN_E_CUDA: return "a CUDA runtime call failed";
         case ATTN_E_TIMEOUT: return "a bounded device wait gave up";
         case ATTN_E_SEQLENS: return "cu_seqlens malformed or a sequence exceeds max_seqlen";
-        case ATTN_E_ARG: return "null pointer or non-finite scale";
+        case ATTN_E_ARG: return "null pointer, non-finite scale or descale, or descale <= 0";
         case ATTN_E_INTERNAL: return "an internal invariant failed on the device";
         case ATTN_E_TOO_LARGE:
             return "problem needs more scratch than attn_bwd_noalloc's built-in 32 MiB array";

@@ -79,6 +79,35 @@ bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64
 // 32 x 1 x 128, 128-byte swizzle; the target of bulk reduce-adds.
 bool make_f32_reduce_map(CUtensorMap* m, void* base, int64_t D, int64_t H, int64_t R);
 
+// fp8 forward: E4M3 q [B,Sq,Hq,D], k [B,Sk,Hkv,D] and V transposed into the
+// workspace as vt [B,Hkv,D,Sk_pad] (Sk_pad = Sk rounded up to 16), one
+// descale factor per tensor; D = 128; out bf16 and lse fp32 contiguous.
+struct Fp8Problem {
+    const uint8_t* q;
+    const uint8_t* k;
+    const uint8_t* v;
+    uint8_t* vt;
+    int64_t q_b, q_s, q_h;      // elements (= bytes)
+    int64_t k_b, k_s, k_h;
+    int64_t v_b, v_s, v_h;
+    int64_t vt_b, vt_h;         // vt: b * vt_b + hk * vt_h + d * Sk_pad + key
+    bf16* out;
+    float* lse;
+    int64_t out_b, out_s, out_h;
+    int64_t lse_b, lse_h;
+    int B, Hq, Hkv, G, Sq, Sk, Sk_pad;
+    int causal;
+    int lazy;
+    float scale_log2;           // scale * descale_q * descale_k * log2(e)
+    float out_scale;            // descale_v
+    int* err;
+};
+
+// TMA tensor map over a 4-D uint8 view (dims innermost first, strides in
+// bytes), box {128, box1, box2, 1}, 128-byte swizzle.
+bool make_u8_map(CUtensorMap* m, const void* base, const int64_t dims[4], const int64_t strides[3],
+                 int box1, int box2);
+
 // Launchers (each enqueues on `stream`, returns cudaGetLastError()).
 cudaError_t launch_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const Problem& p, cudaStream_t stream);
@@ -87,6 +116,8 @@ cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_deterministic(const Problem& p, cudaStream_t stream);
 cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_zero_trailing_bwd(const Problem& p, cudaStream_t stream);
+cudaError_t launch_fp8_transpose_v(const Fp8Problem& p, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const Fp8Problem& p, cudaStream_t stream);
 // One CTA whose thread 0 waits, bounded by budget_ns, on an mbarrier that no
 // one arrives on, and then reports DEV_E_TIMEOUT through `err`.
 cudaError_t launch_wait_timeout_probe(int* err, uint64_t budget_ns, cudaStream_t stream);

@@ -58,4 +58,23 @@ bool make_f32_reduce_map(CUtensorMap* m, void* base, int64_t D, int64_t H, int64
            CUDA_SUCCESS;
 }
 
+bool make_u8_map(CUtensorMap* m, const void* base, const int64_t dims[4], const int64_t strides[3],
+                 int box1, int box2) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[4], st[3];
+    for (int i = 0; i < 4; ++i) d[i] = (cuuint64_t)(dims[i] > 0 ? dims[i] : 1);
+    for (int i = 0; i < 3; ++i) st[i] = (cuuint64_t)strides[i];
+    // Strides of size-1 dims are never used; keep them legal (16-byte multiples).
+    if (d[1] == 1) st[0] = d[0];
+    if (d[2] == 1) st[1] = st[0] * d[1];
+    if (d[3] == 1) st[2] = st[1] * d[2];
+    cuuint32_t box[4] = {128, (cuuint32_t)box1, (cuuint32_t)box2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), d, st, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 }  // namespace attn

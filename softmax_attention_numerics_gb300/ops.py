@@ -17,7 +17,8 @@ from . import _lib
 
 _DT = {torch.bfloat16: _lib.ATTN_BF16, torch.float16: _lib.ATTN_F16,
        torch.float32: _lib.ATTN_F32, torch.int32: _lib.ATTN_I32,
-       torch.uint8: _lib.ATTN_U8, torch.bool: _lib.ATTN_U8}
+       torch.uint8: _lib.ATTN_U8, torch.bool: _lib.ATTN_U8,
+       torch.float8_e4m3fn: _lib.ATTN_E4M3}
 
 
 def tensor_desc(t):
@@ -86,6 +87,43 @@ def attn_fwd(q, k, v, mask=None, cu_seqlens=None, max_seqlen=None, causal=False,
                           _lib.ATTN_EAGER_RESCALE if eager_rescale else 0,
                           ctypes.c_void_p(s.cuda_stream))
     _lib.check(rc, "attn_fwd")
+    return out, lse
+
+
+def fwd_fp8_workspace_bytes(k):
+    lib = _lib.load()
+    return int(lib.attn_fwd_fp8_workspace_bytes(ctypes.byref(tensor_desc(k))))
+
+
+def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, causal=False, scale=None, out=None,
+                 lse=None, workspace=None, eager_rescale=False, stream=None):
+    """Forward on fp8 inputs.  Returns (out, lse).
+
+    q [B,Sq,Hq,128], k/v [B,Sk,Hkv,128]: torch.float8_e4m3fn; real value =
+    element * descale (one float per tensor).  out is bf16 like q's shape,
+    lse fp32 [B,Hq,Sq].  scale=None means 1/sqrt(D).
+    """
+    lib = _lib.load()
+    s = _stream(stream, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    with torch.cuda.device(q.device), torch.cuda.stream(s):
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+        if lse is None:
+            lse = torch.empty(q.shape[0], q.shape[2], q.shape[1], dtype=torch.float32,
+                              device=q.device)
+        nbytes = fwd_fp8_workspace_bytes(k)
+        if workspace is None or workspace.numel() < nbytes:
+            workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+        descs = [tensor_desc(x) for x in (q, k, v, out, lse)]
+        rc = lib.attn_fwd_fp8(*[_ref(d) for d in descs[:3]], float(descale_q), float(descale_k),
+                              float(descale_v), 1 if causal else 0, float(scale),
+                              _ref(descs[3]), _ref(descs[4]),
+                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                              _lib.ATTN_EAGER_RESCALE if eager_rescale else 0,
+                              ctypes.c_void_p(s.cuda_stream))
+    _lib.check(rc, "attn_fwd_fp8")
     return out, lse
 
 

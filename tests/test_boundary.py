@@ -281,6 +281,47 @@ def test_selftest_wait_timeout_rejects_bad_budget(lib):
     assert lib.attn_selftest_wait_timeout(1000001, None) == E["ATTN_E_ARG"]
 
 
+# ---------------------------------------------------------------- fp8 forward
+
+def fp8_dense(B=2, Sq=300, Sk=200, Hq=4, Hkv=2, D=128):
+    E4 = _lib.ATTN_E4M3
+    return dict(q=desc([B, Sq, Hq, D], E4), k=desc([B, Sk, Hkv, D], E4),
+                v=desc([B, Sk, Hkv, D], E4), out=desc([B, Sq, Hq, D]),
+                lse=desc([B, Hq, Sq], _lib.ATTN_F32))
+
+
+def call_fwd_fp8(lib, t, descales=(0.01, 0.02, 0.03), scale=0.1, ws=FAKE, ws_bytes=1 << 40):
+    return lib.attn_fwd_fp8(R(t["q"]), R(t["k"]), R(t["v"]), *descales, 0, scale, R(t["out"]),
+                            R(t["lse"]), ctypes.c_void_p(ws), ws_bytes, 0, None)
+
+
+def test_fp8_forward_contract(lib):
+    stop = (E["ATTN_E_DEVICE"], E["ATTN_E_CUDA"])
+    assert call_fwd_fp8(lib, fp8_dense()) in stop                    # valid: stops at the device
+    t = fp8_dense()
+    t["k"] = desc([2, 200, 2, 128])                                  # bf16 k
+    assert call_fwd_fp8(lib, t) == E["ATTN_E_DTYPE"]
+    t = fp8_dense(D=64)
+    assert call_fwd_fp8(lib, t) == E["ATTN_E_UNSUPPORTED"]
+    t = fp8_dense()
+    t["out"] = desc([2, 300, 4, 128], _lib.ATTN_F32)
+    assert call_fwd_fp8(lib, t) == E["ATTN_E_DTYPE"]
+    t = fp8_dense()
+    t["lse"] = desc([2, 300, 4], _lib.ATTN_F32)                      # transposed lse
+    assert call_fwd_fp8(lib, t) == E["ATTN_E_SHAPE"]
+    t = fp8_dense(Hq=3)
+    assert call_fwd_fp8(lib, t) == E["ATTN_E_SHAPE"]                 # 3 % 2 != 0
+    t = fp8_dense()
+    t["q"] = desc([2, 300, 4, 128], _lib.ATTN_E4M3, stride=[300 * 4 * 136, 4 * 136, 136, 1])
+    assert call_fwd_fp8(lib, t) == E["ATTN_E_LAYOUT"]                # 136-byte rows
+    for bad in ((0.0, 0.02, 0.03), (0.01, -1.0, 0.03), (0.01, 0.02, float("nan"))):
+        assert call_fwd_fp8(lib, fp8_dense(), descales=bad) == E["ATTN_E_ARG"]
+    n = lib.attn_fwd_fp8_workspace_bytes(R(fp8_dense()["k"]))
+    assert n == -(-2 * 2 * 128 * 208 // 256) * 256                  # keys padded to 208
+    assert call_fwd_fp8(lib, fp8_dense(), ws_bytes=n - 1) == E["ATTN_E_WORKSPACE"]
+    assert call_fwd_fp8(lib, fp8_dense(), ws=FAKE + 16, ws_bytes=n) == E["ATTN_E_WORKSPACE"]
+
+
 def test_poisoned_staging_variant_builds_and_exports_the_abi():
     """The race-check debug library (ATTN_POISON_SMEM) compiles for sm_103a
     from the same sources and exports the same C ABI."""
