@@ -193,15 +193,34 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- helpers
 
+# Nominal dense bf16 tensor-core peak of one GB300 (the target is stated against it).
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
 def measured_peaks():
+    """The machine's measured peaks, or the fallback figures, said so on stderr
+    and in every roofline entry ("peak_source")."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(p) as f:
             d = json.load(f)
         return d, "measured"
     except (OSError, ValueError):
+        print("bench.py: %s is missing or unreadable; roofline fractions below are against the "
+              "FALLBACK peaks (6.8 TB/s, 1.9 / 1.7 PFLOP/s bf16)" % p, file=sys.stderr)
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
             "fallback"
+
+
+def peak_fractions(value, peaks, kind):
+    """value (TFLOP/s) against every bf16 denominator: the nominal dense peak
+    (the one the 60 % target names), the burst and the sustained peak."""
+    burst = peaks.get("bf16_tflops", 1900.0)
+    sus = peaks.get("bf16_tflops_sustained", 1700.0)
+    f_nom = value / NOMINAL_BF16_TFLOPS
+    return {"frac_of_nominal_peak": f_nom, "nominal_peak_tflops": NOMINAL_BF16_TFLOPS,
+            "frac_of_burst_peak": value / burst, "frac_of_sustained_peak": value / sus,
+            "peak_source": kind, "target_60pct_of_nominal_met": f_nom >= 0.6}
 
 
 def max_over_ranks(x, device=None):
@@ -323,6 +342,9 @@ def run_fp8_forward(a):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(a.steps)]
     with torch.cuda.stream(stream):
+        for e0, e1 in ev:            # torch creates the CUDA event handles on first record
+            e0.record(stream)
+            e1.record(stream)
         for _ in range(a.warmup):
             step()
     stream.synchronize()
@@ -602,7 +624,8 @@ def main():
                        "causal": a.causal, "parallelism": "replicas" if world > 1 else "single",
                        "l2": "no flush: every input tensor (%d MiB) exceeds L2"
                              % (q.numel() * 2 >> 20),
-                       "frac_of_peak": value / tensor_peak},
+                       "frac_of_peak": value / tensor_peak,
+                       "peaks": peak_fractions(value, peaks, peak_kind)},
             "roofline": roofline,
             "cpu_baseline": cpu_baseline_entry(a, cpu_res) if cpu_res else None,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
