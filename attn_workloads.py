@@ -15,10 +15,13 @@ Workloads (sizes and value distributions as the pages give them):
   (flash-dmattn PR #122, "Problem": seed 42, loss = out.sum()).
 * ``low_lse_row``    B=2, H=4, D=64/128, (Sq, Sk) in {392x392, 360x64,
   100x77, 392x512}, bool / additive / no key-padding mask hiding the last
-  ceil(0.1 Sk) keys; every key gets 36 u added (u a random unit vector) and
-  one query row is -36 u, so that row's LSE sits far below -88.7
+  ceil(0.1 Sk) keys; every key gets c u added (u a random unit vector) and
+  one query row is -c u, so that row's LSE sits far below -88.7
   (OpenWAM PR #64, "Validation": one query row anti-aligned with keys that
-  share a large component).
+  share a large component, row logsumexp about -111 to -120).  c = 37.5
+  puts that row at -112..-118 for D = 128 on every shape and mask kind
+  (c = 36 would leave it at -103..-109); D = 64 keeps the same c (its row
+  then sits at -150..-167).
 * ``wide_spread``    B=2, S=8192, H=32, D=128, k = N(0,1) * s for s in
   {8, 16, 24, 32, 48, 64} (FlyDSL PR #1033, "Repro").
 * ``varlen_gqa``     16 packed sequences, lengths uniform in [128, 4096],
@@ -95,8 +98,13 @@ def padding_mask(B, Sq, Sk, kind, Hq=1, per_row=False, seed=7):
     return add
 
 
-def low_lse_row(Sq, Sk, mask_kind, D=128, row="first", seed=42, B=2, H=4, dtype=BF16):
-    """Keys share 36 u; one query row is -36 u (row LSE far below -88.7)."""
+LOW_ROW_SHARED = 37.5
+
+
+def low_lse_row(Sq, Sk, mask_kind, D=128, row="first", seed=42, B=2, H=4, dtype=BF16,
+                shared=LOW_ROW_SHARED):
+    """Keys share `shared` * u; one query row is -`shared` * u (row LSE far
+    below -88.7)."""
     g = _gen(seed)
     q = _randn(g, (B, Sq, H, D))
     k = _randn(g, (B, Sk, H, D))
@@ -104,9 +112,9 @@ def low_lse_row(Sq, Sk, mask_kind, D=128, row="first", seed=42, B=2, H=4, dtype=
     do = _randn(g, (B, Sq, H, D))
     u = _randn(g, (D,))
     u = u / u.norm()
-    k = k + 36.0 * u
+    k = k + shared * u
     r = 0 if row == "first" else Sq - 1
-    q[:, r, :, :] = -36.0 * u
+    q[:, r, :, :] = -shared * u
     mask = padding_mask(B, Sq, Sk, mask_kind, Hq=H)
     return dict(q=q.to(dtype), k=k.to(dtype), v=v.to(dtype), do=do.to(dtype),
                 causal=False, scale=1.0 / math.sqrt(D), mask=mask, low_row=r)

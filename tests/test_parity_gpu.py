@@ -55,8 +55,11 @@ def test_low_lse_row(shape, mask, row, D):
     assert_finite(res)
     ref = oracle_dense(case)
     r = case["low_row"]
-    # the case really exercises the failure condition: exp(0 - lse) overflows fp32
+    # the case really exercises the failure condition: exp(0 - lse) overflows fp32,
+    # and at D = 128 the row sits where OpenWAM PR #64 (Validation) puts it
     assert ref["lse"][:, :, r].max() < -88.73
+    if D == 128:
+        assert -120.0 <= ref["lse"][:, :, r].min() and ref["lse"][:, :, r].max() <= -110.0
     compare(res, ref, ctx="low_lse %s %s %s D=%d" % (shape, mask, row, D))
     if mask != "none":
         hidden = Sk - math.ceil(0.1 * Sk)
@@ -66,25 +69,66 @@ def test_low_lse_row(shape, mask, row, D):
 
 # ------------------------------------------------------------- wide logit spread
 
-@pytest.mark.parametrize("s", [8, 16, 24, 32, 48, 64])
-def test_wide_spread(s):
-    case = W.wide_spread(s)
-    res = gpu_run(case)
-    assert_finite(res)
+# FlyDSL PR #1033 (Result) reports the output's rel-L2 per K scale for the lazy
+# and the eager rescale; this test measures the same quantities against the fp64
+# oracle (plus the gradients, the lse error and NaN / Inf counted separately
+# over the full tensors) and, when ATTN_REPORT_DIR is set, appends one JSON
+# record per (scale, mode) to wide_spread_report.jsonl there.
+_WIDE_ORACLE = {}
+
+
+def _wide_pairs(s):
     g = torch.Generator().manual_seed(100 + s)
-    pairs = [(int(torch.randint(0, 2, (1,), generator=g)), int(torch.randint(0, 32, (1,), generator=g)))
-             for _ in range(4)]
-    sc = case["scale"]
-    for (b, h) in pairs:
+    return [(int(torch.randint(0, 2, (1,), generator=g)), int(torch.randint(0, 32, (1,), generator=g)))
+            for _ in range(4)]
+
+
+def _wide_oracle(case, s, b, h):
+    key = (s, b, h)
+    if key not in _WIDE_ORACLE:
         qh, kh, vh, dh = (to64(case[n][b, :, h]) for n in ("q", "k", "v", "do"))
-        P, out, lse = O._fwd_head(qh, kh, vh, np.zeros((qh.shape[0], kh.shape[0])), sc)
-        dq, dk, dv = O._bwd_head(qh, kh, vh, P, dh, sc)
+        P, out, lse = O._fwd_head(qh, kh, vh, np.zeros((qh.shape[0], kh.shape[0])), case["scale"])
+        dq, dk, dv = O._bwd_head(qh, kh, vh, P, dh, case["scale"])
         del P
+        _WIDE_ORACLE[key] = dict(out=out, lse=lse, dq=dq, dk=dk, dv=dv)
+    return _WIDE_ORACLE[key]
+
+
+@pytest.mark.parametrize("mode", ["lazy", "eager"])
+@pytest.mark.parametrize("s", [8, 16, 24, 32, 48, 64])
+def test_wide_spread(s, mode):
+    import json
+    import os
+    case = W.wide_spread(s)
+    res = gpu_run(case, eager=mode == "eager")
+    torch.cuda.synchronize()
+    record = {"k_scale": s, "mode": mode, "workload": "B=2 S=8192 H=32 D=128 non-causal bf16",
+              "nan": {}, "inf": {}, "pairs": []}
+    for n in ("out", "lse", "dq", "dk", "dv"):
+        record["nan"][n], record["inf"][n] = nonfinite(res[n])
+    for (b, h) in _wide_pairs(s):
+        ref = _wide_oracle(case, s, b, h)
+        got = {n: to64(res[n][b, :, h]) for n in ("out", "dq", "dk", "dv")}
+        got["lse"] = to64(res["lse"][b, h])
+        record["pairs"].append({
+            "b": b, "h": h,
+            "out_rel_l2": rel_l2(got["out"], ref["out"]),
+            "out_max_abs": float(np.abs(got["out"] - ref["out"]).max()),
+            "lse_max_abs": float(np.abs(got["lse"] - ref["lse"]).max()),
+            **{n + "_rel_l2": rel_l2(got[n], ref[n]) for n in ("dq", "dk", "dv")}})
+        record["pairs"][-1] = {k: (float(v) if isinstance(v, (float, np.floating)) else v)
+                               for k, v in record["pairs"][-1].items()}
+    rdir = os.environ.get("ATTN_REPORT_DIR")
+    if rdir:
+        os.makedirs(rdir, exist_ok=True)
+        with open(os.path.join(rdir, "wide_spread_report.jsonl"), "a") as f:
+            f.write(json.dumps(record) + "\n")
+    print("wide_spread", json.dumps(record))
+    assert_finite(res)
+    for (b, h) in _wide_pairs(s):
         got = {n: res[n][b, :, h] for n in ("out", "dq", "dk", "dv")}
         got["lse"] = res["lse"][b, h]
-        rep = compare(got, dict(out=out, lse=lse, dq=dq, dk=dk, dv=dv),
-                      ctx="wide s=%d (b=%d,h=%d)" % (s, b, h))
-        print("wide_spread s=%d b=%d h=%d %s" % (s, b, h, rep))
+        compare(got, _wide_oracle(case, s, b, h), ctx="wide s=%d %s (b=%d,h=%d)" % (s, mode, b, h))
 
 
 # ------------------------------------------------------------- varlen + GQA + trailing rows
@@ -100,19 +144,17 @@ def test_varlen_gqa():
     assert torch.count_nonzero(res["lse"][:, end:]) == 0
     lens = case["lens"]
     order = sorted(range(len(lens)), key=lambda i: lens[i])
-    pick = [order[0], order[len(order) // 2], order[-1]]
-    heads = [0, 1, 2, 3, 28, 29, 30, 31]          # kv heads 0 and 7, complete groups
+    # every head of four whole sequences: the shortest, two in the middle, the longest
+    pick = [order[0], order[len(order) // 3], order[2 * len(order) // 3], order[-1]]
     for sidx in pick:
         a, e = cu[sidx], cu[sidx + 1]
         sub = {n: case[n][a:e] for n in ("q", "k", "v", "do")}
         out, lse, dq, dk, dv = O.attn_varlen(to64(sub["q"]), to64(sub["k"]), to64(sub["v"]),
                                              to64(sub["do"]), [0, e - a], causal=True,
-                                             scale=case["scale"], heads=heads)
-        got = dict(out=res["out"][a:e, heads], lse=res["lse"][heads, a:e],
-                   dq=res["dq"][a:e, heads], dk=res["dk"][a:e][:, [0, 7]],
-                   dv=res["dv"][a:e][:, [0, 7]])
-        ref = dict(out=out[:, heads], lse=lse[heads], dq=dq[:, heads], dk=dk[:, [0, 7]],
-                   dv=dv[:, [0, 7]])
+                                             scale=case["scale"])
+        got = dict(out=res["out"][a:e], lse=res["lse"][:, a:e], dq=res["dq"][a:e],
+                   dk=res["dk"][a:e], dv=res["dv"][a:e])
+        ref = dict(out=out, lse=lse, dq=dq, dk=dk, dv=dv)
         compare(got, ref, ctx="varlen seq %d (len %d)" % (sidx, e - a))
 
 
