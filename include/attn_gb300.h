@@ -132,6 +132,14 @@ typedef struct {
 /*
  * attn_fwd - forward pass: out and lse.
  *
+ * Defined by the formula above.  Passages it follows: the online softmax
+ * always takes m_new = max(m_row, m_tile) (ROCm/FlyDSL PR #1033, The fix);
+ * the last partial key tile is predicated (OpenWAM PR #64, Root cause);
+ * the exponent is clamped (PFCCLab/cudnn-frontend PR #9, section 3); varlen
+ * rows outside every sequence are written as out = 0, lse = 0 (PFCCLab PR #9,
+ * section 2); all work on the caller's stream (NVIDIA/cudnn-frontend PR #429,
+ * first fix).
+ *
  *   q, k, v     bf16 or fp16 inputs, all three the same type (dense
  *               [B,S,H,D] or varlen [T,H,D]); any other type or a mix gives
  *               ATTN_E_DTYPE before anything is launched.
@@ -189,11 +197,26 @@ size_t attn_fwd_fp8_workspace_bytes(const attn_tensor_t* k);
  * attn_bwd_workspace_bytes - size of the scratch buffer attn_bwd needs for
  * this q / k / flags combination (fp32 dQ accumulator and the per-row
  * Delta and log2-domain lse vectors).  Returns 0 if q or k is malformed.
+ * The caller allocates it, on its own stream: NVIDIA/cudnn-frontend PR #429
+ * (first fix) moves every scratch allocation and zero-fill onto the launch
+ * stream, and flash-dmattn PR #122 (Root Cause 1) requires the accumulator to
+ * start at zero, which attn_bwd does itself on `stream`.
  */
 size_t attn_bwd_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* k, uint32_t flags);
 
 /*
  * attn_bwd - backward pass: dq, dk, dv.
+ *
+ * Defined by the backward formulas above.  Passages it follows: the
+ * probabilities are recomputed with the forward's predicates, the last
+ * partial key tile included (OpenWAM PR #64, Root cause / Fix); the dK / dV
+ * staging tile is handed to the bulk store behind a fence and a barrier
+ * (PFCCLab/cudnn-frontend PR #9, section 1); accumulators start at zero
+ * (flash-dmattn PR #122, Root Cause 1); the deterministic dQ path is
+ * bitwise reproducible and the atomic one stays within the fp32
+ * reassociation bound (PFCCLab PR #9, How it was verified); inputs are
+ * validated against the shape and dtype contract before any launch
+ * (NVIDIA/cudnn-frontend PR #429, the input-validation fixes).
  *
  *   q, k, v, out, dout, lse   as produced / consumed by attn_fwd with the
  *               same mask, cu_seqlens, max_seqlen, causal and scale.
@@ -223,7 +246,11 @@ int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t
  * exceeds 32 MiB (about 64 K (query row, head) pairs at D = 128) are rejected
  * with ATTN_E_TOO_LARGE.  Nothing is allocated or freed by the call.
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make it before any stream capture.
+ * device, with that device current) and may load the library's device code
+ * there; this happens before the arguments are checked, so make the first
+ * call of any kind, valid or not, before any stream capture.  The address is
+ * kept for the life of the process: after cudaDeviceReset() on a device,
+ * this entry point must not be used on that device again.
  * All calls on one device share the array: calls whose work overlaps on the
  * GPU (unordered streams) race on it; order them.  The part that must start
  * at zero is zero-filled on `stream` by every call.
@@ -238,11 +265,15 @@ int attn_bwd_noalloc(const attn_tensor_t* q, const attn_tensor_t* k, const attn_
  * attn_get_error - synchronises `stream`, then returns and clears the error
  * word of the current device: ATTN_OK, ATTN_E_SEQLENS, ATTN_E_TIMEOUT or
  * ATTN_E_INTERNAL
- * (ATTN_E_CUDA if the synchronisation itself failed).
+ * (ATTN_E_CUDA if the synchronisation itself failed).  Device-side faults are
+ * reported rather than hidden, following NVIDIA/cudnn-frontend PR #429
+ * (a clear error instead of silently wrong gradients) and PFCCLab PR #9
+ * (bounded waits instead of a hang).
  */
 int attn_get_error(attn_stream_t stream);
 
-/* attn_strerror - static, human-readable text for a return code. */
+/* attn_strerror - static, human-readable text for a return code (the error
+ * texts NVIDIA/cudnn-frontend PR #429 asks for: say which contract failed). */
 const char* attn_strerror(int code);
 
 /* attn_last_cuda_error - the CUDA runtime error behind the last ATTN_E_CUDA
