@@ -125,9 +125,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             }
             if (*abort_flag) {
                 volatile int no_abort = 0;
-                mbar_wait(bar(L::kBarQ), 0, &no_abort);
+                mbar_wait(bar(L::kBarQ), 0, &no_abort, kDrainBudgetNs);
                 for (int li = max(0, issued - L::kStages); li < issued; ++li)
-                    mbar_wait(bar(L::kBarKVFull + li % L::kStages), (li / L::kStages) & 1, &no_abort);
+                    mbar_wait(bar(L::kBarKVFull + li % L::kStages), (li / L::kStages) & 1, &no_abort, kDrainBudgetNs);
             }
         }
         __syncwarp();
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (!ok) {
                 mma_commit(bar(L::kBarDrain));
                 volatile int no_abort = 0;
-                mbar_wait(bar(L::kBarDrain), 0, &no_abort);
+                mbar_wait(bar(L::kBarDrain), 0, &no_abort, kDrainBudgetNs);
             }
         }
         __syncwarp();

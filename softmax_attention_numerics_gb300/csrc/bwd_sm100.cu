@@ -220,9 +220,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
         }
         if (*abort_flag && lane == 0) {
             volatile int no_abort = 0;
-            mbar_wait(bar(L::kBarKV), 0, &no_abort);
+            mbar_wait(bar(L::kBarKV), 0, &no_abort, kDrainBudgetNs);
             for (int it = max(0, issued - 2); it < issued; ++it)
-                mbar_wait(bar(L::kBarQFull + (it & 1)), (it >> 1) & 1, &no_abort);
+                mbar_wait(bar(L::kBarQFull + (it & 1)), (it >> 1) & 1, &no_abort, kDrainBudgetNs);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_sm100_kernel(const Problem
             if (!ok) {
                 mma_commit(bar(L::kBarDrain));
                 volatile int no_abort = 0;
-                mbar_wait(bar(L::kBarDrain), 0, &no_abort);
+                mbar_wait(bar(L::kBarDrain), 0, &no_abort, kDrainBudgetNs);
             }
         }
         __syncwarp();

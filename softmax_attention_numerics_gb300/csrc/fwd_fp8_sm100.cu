@@ -163,10 +163,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             if (*abort_flag) {
                 // Let every copy in flight (the Q tiles too) land before the CTA exits.
                 volatile int no_abort = 0;
-                mbar_wait(bar(L::kBarQ), 0, &no_abort);
+                mbar_wait(bar(L::kBarQ), 0, &no_abort, kDrainBudgetNs);
                 for (int li = max(0, issued - L::kStages); li < issued; ++li) {
                     const int s = li % L::kStages, r = li / L::kStages;
-                    mbar_wait(bar(L::kBarKVFull + s), r & 1, &no_abort);
+                    mbar_wait(bar(L::kBarKVFull + s), r & 1, &no_abort, kDrainBudgetNs);
                 }
             }
         }
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             if (!ok) {
                 mma_commit(bar(L::kBarDrain));
                 volatile int no_abort = 0;
-                mbar_wait(bar(L::kBarDrain), 0, &no_abort);
+                mbar_wait(bar(L::kBarDrain), 0, &no_abort, kDrainBudgetNs);
             }
         }
         __syncwarp();

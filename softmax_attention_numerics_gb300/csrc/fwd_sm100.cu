@@ -145,11 +145,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             }
             if (*abort_flag) {
-                // Let the copies in flight land before the CTA exits.
+                // Let the copies in flight (the Q tiles too) land before the CTA exits.
+                volatile int no_abort = 0;
+                mbar_wait(bar(L::kBarQ), 0, &no_abort, kDrainBudgetNs);
                 for (int li = max(0, issued - L::kStages); li < issued; ++li) {
                     const int s = li % L::kStages, r = li / L::kStages;
-                    volatile int no_abort = 0;
-                    mbar_wait(bar(L::kBarKVFull + s), r & 1, &no_abort);
+                    mbar_wait(bar(L::kBarKVFull + s), r & 1, &no_abort, kDrainBudgetNs);
                 }
             }
         }
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!ok) {
                 mma_commit(bar(L::kBarDrain));
                 volatile int no_abort = 0;
-                mbar_wait(bar(L::kBarDrain), 0, &no_abort);
+                mbar_wait(bar(L::kBarDrain), 0, &no_abort, kDrainBudgetNs);
             }
         }
         __syncwarp();

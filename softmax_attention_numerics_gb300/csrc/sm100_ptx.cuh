@@ -27,6 +27,10 @@ __device__ __forceinline__ uint64_t global_ns() {
 // A single wait may legitimately last as long as one tile's work; two
 // seconds is orders of magnitude beyond that.
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;
+// Waits of the unwind path, for copies and MMAs that are already in flight
+// (they complete without any further action of this CTA), keep this long
+// budget so that no CTA exits while the async units still write its memory.
+constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 
 // ------------------------------------------------------------------ mbarrier
 
