@@ -90,6 +90,45 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// ------------------------------------------------------------------ debug build
+
+// Debug builds only (ATTN_DEBUG_CHECKS; the product build compiles both hooks
+// to nothing).  dbg_check records ATTN_E_INTERNAL for a failed per-tile
+// bounds check and returns false so that the caller skips the access (a
+// skipped copy or MMA then makes a later wait run out, and the kernel
+// unwinds).  dbg_stall makes one bounded wait of one block's MMA issuer,
+// chosen by (kernel, iteration), run out on a barrier that nothing
+// completes at that point, so that the kernel's own unwind paths run:
+// the abort flag, the drains of copies and MMAs in flight, ATTN_E_TIMEOUT.
+constexpr uint64_t kDebugStallBudgetNs = 200000ull;     // 200 us
+enum { kStallFwd = 1, kStallBwd = 2, kStallDq = 3, kStallFp8 = 4 };
+
+__device__ __forceinline__ bool dbg_check(bool ok, int* err) {
+#ifdef ATTN_DEBUG_CHECKS
+    if (!ok) set_error(err, DEV_E_INTERNAL);
+    return ok;
+#else
+    (void)ok;
+    (void)err;
+    return true;
+#endif
+}
+
+__device__ __forceinline__ bool dbg_stall(int stall_at, int kernel, int it, uint32_t never_bar,
+                                          volatile int* abort_flag) {
+#ifdef ATTN_DEBUG_CHECKS
+    if (stall_at == ((kernel << 16) | it) && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        return mbar_wait(never_bar, 0, abort_flag, kDebugStallBudgetNs);
+#else
+    (void)stall_at;
+    (void)kernel;
+    (void)it;
+    (void)never_bar;
+    (void)abort_flag;
+#endif
+    return true;
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
