@@ -297,6 +297,21 @@ int attn_version(void);
 int attn_selftest_wait_timeout(uint32_t budget_us, attn_stream_t stream);
 
 /*
+ * Debug builds (not part of this ABI).  The build script makes two debug
+ * variants of the library from the same sources.  In the poisoned-staging
+ * build every writer of a backward staging tile first stores NaN into it,
+ * so a consumer that reads the tile too early yields NaN gradients.  The
+ * checked build adds per-tile bounds checks that record ATTN_E_INTERNAL and
+ * skip the access instead of trapping, and exports one more function,
+ * int attn_debug_inject_stall(int kernel, int iteration): from then on the
+ * MMA issuer of block (0, 0, 0) of `kernel` (1 forward, 2 backward main,
+ * 3 deterministic dQ, 4 fp8 forward) lets its wait at loop iteration
+ * `iteration` (0 .. 65535) run out after 200 us, so that the kernel unwinds
+ * and reports ATTN_E_TIMEOUT; kernel <= 0 turns it off; ATTN_E_ARG for
+ * arguments out of range.
+ */
+
+/*
  * Profiling hooks (used by the benchmark; no effect on results).
  *
  * attn_profile_events - from now on, record the CUDA events `before` and

@@ -52,13 +52,23 @@ def up_to_date(lib: str = LIB) -> bool:
 # the tile before the writes have landed produces non-finite output.
 POISON_LIB = os.path.join(LIB_DIR, "libattn_gb300_poison.so")
 
+# Debug variant: per-tile bounds checks that record ATTN_E_INTERNAL and skip
+# the access instead of trapping, and attn_debug_inject_stall(), which makes
+# one bounded wait of one block's MMA issuer run out so that the kernels' own
+# unwind paths (abort flag, drains, ATTN_E_TIMEOUT) run on the GPU.
+CHECKED_LIB = os.path.join(LIB_DIR, "libattn_gb300_checked.so")
+
 
 def build(force: bool = False, verbose: bool = False, extra_flags=(), variant=None) -> str:
-    """variant None: the library; "poison": the poisoned-staging debug build."""
+    """variant None: the library; "poison": the poisoned-staging debug build;
+    "checked": the bounds-check / stall-injection debug build."""
     out_lib, build_dir = LIB, BUILD
     if variant == "poison":
         out_lib, build_dir = POISON_LIB, os.path.join(BUILD, "poison")
         extra_flags = tuple(extra_flags) + ("-DATTN_POISON_SMEM",)
+    elif variant == "checked":
+        out_lib, build_dir = CHECKED_LIB, os.path.join(BUILD, "checked")
+        extra_flags = tuple(extra_flags) + ("-DATTN_DEBUG_CHECKS",)
     elif variant is not None:
         raise ValueError("unknown build variant %r" % (variant,))
     if not force and up_to_date(out_lib):

@@ -41,6 +41,7 @@ int* error_word(int dev) {
 }
 
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<int> g_debug_stall{-1};
 thread_local char g_cuda_detail[256] = "";
 
 int cuda_fail(cudaError_t e, const char* what) {
@@ -292,6 +293,7 @@ int fill_common(Problem* p, const Shapes& s, const attn_tensor_t* q, const attn_
     p->scale = scale;
     p->scale_log2 = scale * 1.4426950408889634f;
     p->lazy = (flags & ATTN_EAGER_RESCALE) ? 0 : 1;
+    p->debug_stall = debug_stall_point();
     return ATTN_OK;
 }
 
@@ -330,6 +332,9 @@ WsLayout ws_layout(const Shapes& s, uint32_t flags) {
 
 
 }  // namespace
+
+int debug_stall_point() { return g_debug_stall.load(std::memory_order_relaxed); }
+
 }  // namespace attn
 
 using namespace attn;
@@ -437,6 +442,7 @@ extern "C" int attn_fwd_fp8(const attn_tensor_t* q, const attn_tensor_t* k, cons
     p.lazy = (flags & ATTN_EAGER_RESCALE) ? 0 : 1;
     p.scale_log2 = scale * descale_q * descale_k * 1.4426950408889634f;
     p.out_scale = descale_v;
+    p.debug_stall = debug_stall_point();
     int dev;
     ATTN_TRY(current_device(&dev));
     for (const attn_tensor_t* t : {q, k, v, static_cast<const attn_tensor_t*>(out),
@@ -588,3 +594,18 @@ extern "C" const char* attn_last_cuda_error(void) { return g_cuda_detail; }
 extern "C" unsigned long long attn_launch_count(void) {
     return g_launches.load(std::memory_order_relaxed);
 }
+
+#ifdef ATTN_DEBUG_CHECKS
+// Debug builds only: from now on, the MMA issuer of block (0, 0, 0) of
+// `kernel` (1 forward, 2 backward main, 3 deterministic dQ, 4 fp8 forward)
+// lets its wait at iteration `iteration` run out; kernel <= 0 clears it.
+extern "C" int attn_debug_inject_stall(int kernel, int iteration) {
+    if (kernel <= 0) {
+        g_debug_stall.store(-1);
+        return ATTN_OK;
+    }
+    if (kernel > 4 || iteration < 0 || iteration > 0xffff) return ATTN_E_ARG;
+    g_debug_stall.store((kernel << 16) | iteration);
+    return ATTN_OK;
+}
+#endif

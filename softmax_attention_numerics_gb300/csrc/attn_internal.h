@@ -62,12 +62,16 @@ struct Problem {
     float scale_log2;   // scale * log2(e)
     int lazy;           // 1: lazy rescale with threshold 8 (log2 units)
     int* err;           // device error word
+    int debug_stall;    // debug builds: (kernel << 16 | iteration) whose wait runs out; -1 none
 };
 
 // Error codes written to the device error word (match include/attn_gb300.h).
 constexpr int DEV_E_TIMEOUT = -8;
 constexpr int DEV_E_SEQLENS = -9;
 constexpr int DEV_E_INTERNAL = -11;
+
+// Debug builds: the stall point set by attn_debug_inject_stall (-1: none).
+int debug_stall_point();
 
 // TMA tensor map over a 16-bit (bf16, or fp16 when f16) [B, S, H, D] view
 // (dims innermost first: D, H, S, B; strides in elements), box 64 x 1 x 128 x 1,
@@ -101,6 +105,7 @@ struct Fp8Problem {
     float scale_log2;           // scale * descale_q * descale_k * log2(e)
     float out_scale;            // descale_v
     int* err;
+    int debug_stall;            // as in Problem
 };
 
 // TMA tensor map over a 4-D uint8 view (dims innermost first, strides in

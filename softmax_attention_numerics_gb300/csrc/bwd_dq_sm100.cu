@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 }
             }
             for (int j = 0; ok && j < n; ++j) {
+                if (!(ok = dbg_stall(p.debug_stall, kStallDq, j, bar(L::kBarDrain), abort_flag))) break;
                 const bool next = j + 1 < n;
                 if (next) {
                     // S_{j+1} goes into the buffer dQ_{j-1} read dS_{j-1} from.

@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     const int li = 2 * j + which;
                     const int s = li % L::kStages, r = li / L::kStages;
                     if (!mbar_wait(bar(L::kBarKVEmpty + s), (r & 1) ^ 1, abort_flag)) break;
+                    if (!dbg_check(j * kF8Tile < p.Sk && s < L::kStages, p.err)) break;
                     mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kTileBytes);
                     const uint32_t dst = sbase + L::kKV + s * L::kTileBytes;
                     if (which == 0)   // K_j: keys j*128.., all D bytes
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 }
             }
             for (int j = 0; ok && j < n_all; ++j) {
+                if (!(ok = dbg_stall(p.debug_stall, kStallFp8, j, bar(L::kBarDrain), abort_flag))) break;
                 const int lv = 2 * j + 1, lk = 2 * j + 2;
                 if (!(ok = mbar_wait(bar(L::kBarKVFull + kv_stage(lv)), kv_par(lv), abort_flag))) break;
                 const bool next = j + 1 < n_all;

@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     const int li = 2 * j + which;
                     const int s = li % L::kStages, r = li / L::kStages;
                     if (!mbar_wait(bar(L::kBarKVEmpty + s), (r & 1) ^ 1, abort_flag)) break;
+                    // every key tile starts inside the sequence (debug builds check it)
+                    if (!dbg_check(j * kTile < si.len_k && s < L::kStages, p.err)) break;
                     mbar_arrive_expect_tx(bar(L::kBarKVFull + s), L::kTileBytes);
                     const CUtensorMap* m = which ? &maps.v : &maps.k;
 #pragma unroll
@@ -164,6 +166,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const uint32_t colO[2] = {L::kColO0, L::kColO1};
             auto kv_stage = [&](int li) { return li % L::kStages; };
             auto kv_par = [&](int li) { return (uint32_t)((li / L::kStages) & 1); };
+            // TMEM columns of every accumulator stay inside the allocation
+            dbg_check(L::kColS1 + kTile <= L::kTmemCols && L::kColO1 + D <= L::kTmemCols, p.err);
             auto issue_qk = [&](int t, int j) {
                 const int s = kv_stage(2 * j);
                 const uint64_t qd = smem_desc(sbase + L::kQ + t * L::kTileBytes, 16, 1024, kSwizzle128B);
@@ -198,6 +202,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             }
             for (int j = 0; ok && j < n_all; ++j) {
+                if (!(ok = dbg_stall(p.debug_stall, kStallFwd, j, bar(L::kBarDrain), abort_flag))) break;
                 const int lv = 2 * j + 1, lk = 2 * j + 2;
                 if (!(ok = mbar_wait(bar(L::kBarKVFull + kv_stage(lv)), kv_par(lv), abort_flag)))
                     break;

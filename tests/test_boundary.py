@@ -335,6 +335,32 @@ def test_poisoned_staging_variant_builds_and_exports_the_abi():
         build.build(variant="nonexistent")
 
 
+def test_checked_variant_builds_and_exports_the_abi_and_the_stall_hook():
+    """The bounds-check / stall-injection debug library (ATTN_DEBUG_CHECKS)
+    compiles from the same sources, exports the same C ABI plus
+    attn_debug_inject_stall, which the product library does not export;
+    the hook only sets a host-side value and validates its arguments."""
+    path = build.build(variant="checked")
+    assert path == build.CHECKED_LIB and os.path.exists(path)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True,
+                         text=True).stdout
+    for name in declared_functions():
+        assert re.search(r"\bT %s\b" % name, out), name
+    assert re.search(r"\bT attn_debug_inject_stall\b", out)
+    prod = subprocess.run(["nm", "-D", "--defined-only", build.build()], capture_output=True,
+                          text=True).stdout
+    assert not re.search(r"\battn_debug_inject_stall\b", prod)
+    dbg = ctypes.CDLL(path)
+    fn = dbg.attn_debug_inject_stall
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_int, ctypes.c_int]
+    assert fn(5, 0) == E["ATTN_E_ARG"]
+    assert fn(1, -1) == E["ATTN_E_ARG"]
+    assert fn(2, 70000) == E["ATTN_E_ARG"]
+    assert fn(2, 3) == 0
+    assert fn(0, 0) == 0
+
+
 def test_use_library_swaps_and_restores(lib):
     """Calls inside `use_library` go through the named build; the previous
     library comes back afterwards, also when the block raises."""
