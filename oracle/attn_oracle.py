@@ -38,6 +38,10 @@ What it computes (the definition that every page relies on):
 * fp8 inputs: E4M3 codes with one descale factor per tensor are decoded
   from the format's definition and the forward is the same definition on
   the decoded values (FlyDSL PR #1033, "The fp8 helper, second commit").
+* attention targets recomputed from the forward's lse and summed over the
+  query heads, with the exponent clamped at 120, and each row's L1 norm
+  (PFCCLab/cudnn-frontend PR #9, sections 2 and 3: the dense score
+  recompute that produces the targets of a sparse-attention indexer).
 
 Layouts follow the library: q/out/dout [B, Sq, Hq, D]; k/v [B, Sk, Hkv, D];
 lse [B, Hq, Sq]; varlen q [T, Hq, D], k/v [T, Hkv, D], lse [Hq, T].
@@ -51,6 +55,7 @@ import math
 import numpy as np
 
 __all__ = [
+    "attn_score_recompute",
     "attn_fwd",
     "attn_fwd_fp8",
     "e4m3_decode",
@@ -276,3 +281,68 @@ def attn_fwd_fp8(q_codes, k_codes, v_codes, descale_q, descale_k, descale_v, cau
     k = e4m3_decode(k_codes) * float(descale_k)
     v = e4m3_decode(v_codes) * float(descale_v)
     return attn_fwd(q, k, v, causal=causal, scale=scale)
+
+
+# ---------------------------------------------------------------- score recompute
+
+SCORE_CLAMP_LOG2 = 120.0
+
+
+def _score_terms(qh, kh, lse_h, bias, scale):
+    """One (batch or sequence, q head): exp2(min(log2(e) (s - lse), 120)),
+    [rows, keys]; hidden pairs (bias -inf) give exactly 0."""
+    s = scale * (qh @ kh.T) + bias
+    t = np.log2(np.e) * (s - lse_h[:, None])
+    return np.exp2(np.minimum(t, SCORE_CLAMP_LOG2))
+
+
+def attn_score_recompute(q, k, lse, causal=False, scale=None, cu_seqlens=None, max_seqlen=None):
+    """Attention targets recomputed from the forward's lse, summed over heads.
+
+    PFCCLab/cudnn-frontend PR #9, section 3 (the dense score recompute): for a
+    query row i and a key j of its sequence,
+        score_ij = sum over q heads h of exp2(min(log2(e) (s_hij - lse_hi), 120))
+    with s_hij = scale q_hi . k_j (k of h's kv head; hidden pairs - causal
+    j > i - contribute 0), and the row's L1 norm l1_i = sum_j score_ij; the
+    consumer's target is score_ij / l1_i.  The clamp bounds every term by
+    2^120 so that the sum over heads stays finite (2^120 * 64 < FLT_MAX) even
+    when an lse is far too small; with the forward's own lse each head's
+    terms over j sum to 1, so l1_i is the number of heads with a visible key.
+    Section 2: rows that no tile visits (varlen rows past cu[-1]) come back
+    as 0, not -inf, in both outputs.
+
+    dense:  q [B,Sq,Hq,D], k [B,Sk,Hkv,D], lse [B,Hq,Sq] -> score [B,Sq,Sk], l1 [B,Sq]
+    varlen: q [T,Hq,D], k [T,Hkv,D], lse [Hq,T], cu_seqlens [n+1] ->
+            score [T, max_seqlen] (row cu[s] + i holds keys 0.. of sequence s;
+            columns past the sequence are 0), l1 [T]
+    """
+    q, k, lse = _as64(q), _as64(k), _as64(lse)
+    if cu_seqlens is None:
+        B, Sq, Hq, D = q.shape
+        Sk, Hkv = k.shape[1], k.shape[2]
+        G = Hq // Hkv
+        sc = _default_scale(D, scale)
+        score = np.zeros((B, Sq, Sk))
+        for b in range(B):
+            bias = bias_for(None, 0, 0, Sq, Sk, causal)
+            for h in range(Hq):
+                score[b] += _score_terms(q[b, :, h], k[b, :, h // G], lse[b, h], bias, sc)
+        return score, score.sum(axis=2)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    sc = _default_scale(D, scale)
+    cu = [int(x) for x in cu_seqlens]
+    W = int(max_seqlen) if max_seqlen is not None else max(
+        [cu[i + 1] - cu[i] for i in range(len(cu) - 1)] + [0])
+    score = np.zeros((T, W))
+    for si in range(len(cu) - 1):
+        a, e = cu[si], cu[si + 1]
+        L = e - a
+        if L == 0:
+            continue
+        bias = bias_for(None, 0, 0, L, L, causal)
+        for h in range(Hq):
+            score[a:e, :L] += _score_terms(q[a:e, h], k[a:e, h // G], lse[h, a:e], bias, sc)
+    return score, score.sum(axis=1)
+

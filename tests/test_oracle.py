@@ -582,3 +582,102 @@ def test_pins_catch_missing_max_in_lse(monkeypatch):
     monkeypatch.setattr(O, "_fwd_head", bad)
     with pytest.raises(AssertionError):
         test_constant_logit_shift()
+
+
+# ---------------------------------------------------------------- score recompute
+
+def _score_case(seed, B=2, Sq=9, Sk=11, Hq=4, Hkv=2, D=8):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((B, Sq, Hq, D)), rng.standard_normal((B, Sk, Hkv, D)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_score_l1_norm_is_the_head_count(causal):
+    """With the forward's own lse every head's terms of a row sum to 1, so
+    the L1 norm of the head-summed scores is the number of heads
+    (PFCCLab/cudnn-frontend PR #9, How it was verified: a leaked 64.0 is a
+    previous attn_l1norm of 64 heads)."""
+    q, k = _score_case(40)
+    _, lse = O.attn_fwd(q, k, k, causal=causal, scale=0.3)
+    score, l1 = O.attn_score_recompute(q, k, lse, causal=causal, scale=0.3)
+    assert np.allclose(l1, q.shape[2], rtol=1e-12, atol=0)
+    assert (score >= 0).all()
+
+
+def test_score_is_the_head_sum_of_attention_weights():
+    """score_ij equals the sum over heads of the softmax weights the forward
+    computes (a different route: exact row max, then normalise)."""
+    q, k = _score_case(41, Sq=7, Sk=7)
+    _, lse = O.attn_fwd(q, k, k, causal=True, scale=0.45)
+    score, _ = O.attn_score_recompute(q, k, lse, causal=True, scale=0.45)
+    ref = np.zeros_like(score)
+    G = q.shape[2] // k.shape[2]
+    for b in range(q.shape[0]):
+        bias = O.bias_for(None, 0, 0, 7, 7, True)
+        for h in range(q.shape[2]):
+            P, _, _ = O._fwd_head(q[b, :, h], k[b, :, h // G], k[b, :, h // G], bias, 0.45)
+            ref[b] += P
+    assert np.allclose(score, ref, rtol=1e-12, atol=1e-15)
+    j, i = np.meshgrid(np.arange(7), np.arange(7))
+    assert (score[:, j > i] == 0).all()                # causal pairs get exactly 0
+
+
+def test_score_clamp_keeps_a_degenerate_lse_finite():
+    """PFCCLab/cudnn-frontend PR #9, section 3: an lse far too small (the
+    -1e30 mask constant) makes every term exp2(+huge); the clamp at 120 keeps
+    each at 2^120 and the sum over heads finite (2^120 * 64 < FLT_MAX)."""
+    q, k = _score_case(42, Hq=64, Hkv=1)
+    _, lse = O.attn_fwd(q, k, k, scale=0.3)
+    lse[0, :, 3] = -1e30                              # one degenerate row, every head
+    score, l1 = O.attn_score_recompute(q, k, lse, scale=0.3)
+    assert np.isfinite(score).all() and np.isfinite(l1).all()
+    assert (score[0, 3] == 64 * 2.0 ** 120).all()
+    assert np.float32(64 * 2.0 ** 120) < np.finfo(np.float32).max
+    others = np.delete(l1, 3, axis=1)
+    assert np.allclose(others, 64, rtol=1e-12)
+
+
+def test_score_varlen_layout_and_unvisited_rows():
+    """Varlen: row cu[s] + i holds sequence s's keys in columns 0..len-1 and
+    0 beyond; rows past cu[-1] are 0 in both outputs (section 2: 0, not
+    -inf); each sequence equals the dense problem on its own rows."""
+    rng = np.random.default_rng(43)
+    cu = [0, 5, 5, 12]
+    T, Hq, Hkv, D = 15, 4, 2, 8
+    q, k = rng.standard_normal((T, Hq, D)), rng.standard_normal((T, Hkv, D))
+    out, lse, *_ = O.attn_varlen(q, k, k, np.zeros_like(q), cu, causal=True, scale=0.4)
+    score, l1 = O.attn_score_recompute(q, k, lse, causal=True, scale=0.4, cu_seqlens=cu,
+                                       max_seqlen=8)
+    assert score.shape == (T, 8) and l1.shape == (T,)
+    assert (score[12:] == 0).all() and (l1[12:] == 0).all()
+    assert (score[0:5, 5:] == 0).all()
+    assert np.allclose(l1[:12], Hq, rtol=1e-12)
+    a, e = 5, 12
+    _, lse_d = O.attn_fwd(q[None, a:e], k[None, a:e], k[None, a:e], causal=True, scale=0.4)
+    sd, _ = O.attn_score_recompute(q[None, a:e], k[None, a:e], lse_d, causal=True, scale=0.4)
+    assert np.allclose(score[a:e, :7], sd[0], rtol=1e-12)
+
+
+def test_score_pins_catch_planted_mistakes(monkeypatch):
+    """A missing clamp, a dropped lse or exp in place of exp2 each fail a pin."""
+    orig = O._score_terms
+
+    def no_clamp(qh, kh, lse_h, bias, scale):
+        s = scale * (qh @ kh.T) + bias
+        return np.exp2(np.log2(np.e) * (s - lse_h[:, None]))
+
+    def no_lse(qh, kh, lse_h, bias, scale):
+        return orig(qh, kh, np.zeros_like(lse_h), bias, scale)
+
+    def exp_not_exp2(qh, kh, lse_h, bias, scale):
+        s = scale * (qh @ kh.T) + bias
+        return np.exp(np.minimum(np.log2(np.e) * (s - lse_h[:, None]), 120.0))
+
+    with np.errstate(over="ignore"):
+        monkeypatch.setattr(O, "_score_terms", no_clamp)
+        with pytest.raises(AssertionError):
+            test_score_clamp_keeps_a_degenerate_lse_finite()
+    for bad in (no_lse, exp_not_exp2):
+        monkeypatch.setattr(O, "_score_terms", bad)
+        with pytest.raises(AssertionError):
+            test_score_l1_norm_is_the_head_count(False)
