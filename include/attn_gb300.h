@@ -262,6 +262,44 @@ int attn_bwd_noalloc(const attn_tensor_t* q, const attn_tensor_t* k, const attn_
                      attn_tensor_t* dv, uint32_t flags, attn_stream_t stream);
 
 /*
+ * attn_score_recompute - attention targets recomputed from the forward's lse
+ * and summed over the query heads, with each row's L1 norm.
+ *
+ * Follows PFCCLab/cudnn-frontend PR #9, section 3 (the dense score recompute
+ * behind a sparse-attention indexer's training targets) and section 2 (rows
+ * no tile visits are written as 0, not -inf):
+ *
+ *   score_ij = sum_h exp2(min(log2(e) (scale q_hi . k_j - lse_hi), 120))
+ *   l1_i     = sum_j score_ij          (the consumer's target: score / l1)
+ *
+ * The clamp bounds each term by 2^120 so that the sum over heads stays
+ * finite when an lse is far too small; with the forward's own lse it never
+ * fires and l1_i is the number of heads.  Hidden pairs (causal j > i) add 0.
+ *
+ *   q, k        as for attn_fwd (bf16 or fp16, D = 64 or 128, GQA allowed);
+ *               no mask.
+ *   lse         fp32, as attn_fwd wrote it: [B,Hq,Sq] or [Hq,T].
+ *   cu_seqlens, max_seqlen, causal, scale   as for attn_fwd.
+ *   score       fp32, contiguous: dense [B,Sq,Sk]; varlen [T,max_seqlen], row
+ *               cu[s] + i holding sequence s's keys in columns 0..len-1 and 0
+ *               past them; rows >= cu[nseq] are 0.  Fully written.
+ *   l1          fp32, contiguous: dense [B,Sq]; varlen [T].  Fully written.
+ *   workspace   attn_score_workspace_bytes() bytes, 256-byte aligned (per
+ *               key-tile partial sums, added in a fixed order so that both
+ *               outputs are bit-reproducible).
+ *   flags       0.
+ */
+int attn_score_recompute(const attn_tensor_t* q, const attn_tensor_t* k, const attn_tensor_t* lse,
+                         const attn_tensor_t* cu_seqlens, int32_t max_seqlen, int causal,
+                         float scale, attn_tensor_t* score, attn_tensor_t* l1, void* workspace,
+                         size_t workspace_bytes, uint32_t flags, attn_stream_t stream);
+
+/* attn_score_workspace_bytes - workspace attn_score_recompute needs (0 if q or
+ * k is malformed). */
+size_t attn_score_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* k,
+                                  const attn_tensor_t* cu_seqlens, int32_t max_seqlen);
+
+/*
  * attn_get_error - synchronises `stream`, then returns and clears the error
  * word of the current device: ATTN_OK, ATTN_E_SEQLENS, ATTN_E_TIMEOUT or
  * ATTN_E_INTERNAL
@@ -305,7 +343,7 @@ int attn_selftest_wait_timeout(uint32_t budget_us, attn_stream_t stream);
  * skip the access instead of trapping, and exports one more function,
  * int attn_debug_inject_stall(int kernel, int iteration): from then on the
  * MMA issuer of block (0, 0, 0) of `kernel` (1 forward, 2 backward main,
- * 3 deterministic dQ, 4 fp8 forward) lets its wait at loop iteration
+ * 3 deterministic dQ, 4 fp8 forward, 5 score recompute) lets its wait at loop iteration
  * `iteration` (0 .. 65535) run out after 200 us, so that the kernel unwinds
  * and reports ATTN_E_TIMEOUT; kernel <= 0 turns it off; ATTN_E_ARG for
  * arguments out of range.
@@ -325,7 +363,8 @@ enum {
     ATTN_STAGE_BWD_PREPROCESS = 1, /* Delta = rowsum(dO o out), lse2         */
     ATTN_STAGE_BWD_MAIN = 2,       /* dK, dV (and atomic dQ partials)        */
     ATTN_STAGE_BWD_DQ = 3,         /* dQ convert, or the deterministic dQ    */
-    ATTN_STAGE_COUNT = 4
+    ATTN_STAGE_SCORE = 4,          /* score recompute (then its L1 reduce)   */
+    ATTN_STAGE_COUNT = 5
 };
 int attn_profile_events(int stage, void* before, void* after);
 

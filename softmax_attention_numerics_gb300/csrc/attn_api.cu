@@ -533,6 +533,71 @@ extern "C" int attn_bwd(const attn_tensor_t* q, const attn_tensor_t* k, const at
     return run_stage(ATTN_STAGE_BWD_DQ, st, [&] { return launch_bwd_dq_convert(p, st); });
 }
 
+// ------------------------------------------------------------------ score recompute
+
+namespace attn {
+namespace {
+
+// Rows and width of the score output and the L1-partial workspace size.
+void score_dims(const Shapes& s, int64_t* rows, int64_t* width) {
+    *rows = s.varlen ? s.T : s.B * s.Sq;
+    *width = s.varlen ? s.Sq : s.Sk;
+}
+
+size_t score_workspace(const Shapes& s) {
+    int64_t rows, width;
+    score_dims(s, &rows, &width);
+    return round256(static_cast<size_t>(score_key_tiles(width)) * static_cast<size_t>(rows) * 4);
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" size_t attn_score_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* k,
+                                             const attn_tensor_t* cu_seqlens, int32_t max_seqlen) {
+    Shapes s;
+    if (!q || !k) return 0;
+    if (derive_shapes(q, k, k, cu_seqlens, max_seqlen, &s) != ATTN_OK) return 0;
+    return score_workspace(s);
+}
+
+extern "C" int attn_score_recompute(const attn_tensor_t* q, const attn_tensor_t* k,
+                                    const attn_tensor_t* lse, const attn_tensor_t* cu_seqlens,
+                                    int32_t max_seqlen, int causal, float scale,
+                                    attn_tensor_t* score, attn_tensor_t* l1, void* workspace,
+                                    size_t workspace_bytes, uint32_t flags,
+                                    attn_stream_t stream) {
+    if (flags != 0) return ATTN_E_ARG;
+    Shapes s;
+    ATTN_TRY(derive_shapes(q, k, k, cu_seqlens, max_seqlen, &s));
+    // lse is read in the layout attn_fwd wrote it
+    ATTN_TRY(check_output(lse, ATTN_F32, s.lse_shape, s.lse_rank));
+    int64_t rows, width;
+    score_dims(s, &rows, &width);
+    const int64_t sshape_d[3] = {s.B, s.Sq, s.Sk};
+    const int64_t sshape_v[2] = {s.T, s.Sq};
+    ATTN_TRY(check_output(score, ATTN_F32, s.varlen ? sshape_v : sshape_d, s.varlen ? 2 : 3));
+    const int64_t lshape_d[2] = {s.B, s.Sq};
+    const int64_t lshape_v[1] = {s.T};
+    ATTN_TRY(check_output(l1, ATTN_F32, s.varlen ? lshape_v : lshape_d, s.varlen ? 1 : 2));
+    const size_t need = score_workspace(s);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return ATTN_E_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_E_WORKSPACE;
+    }
+    Problem p;
+    ATTN_TRY(fill_common(&p, s, q, k, k, nullptr, cu_seqlens, causal, scale, 0));
+    ATTN_TRY(bind_device(&p, {q, k, lse, cu_seqlens, score, l1}));
+    p.lse = static_cast<float*>(lse->data);
+    p.score = static_cast<float*>(score->data);
+    p.l1 = static_cast<float*>(l1->data);
+    p.l1_part = static_cast<float*>(workspace);
+    p.sc_w = width;
+    p.l1_rows = rows;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return run_stage(ATTN_STAGE_SCORE, st, [&] { return launch_score_recompute(p, st); });
+}
+
 extern "C" int attn_get_error(attn_stream_t stream) {
     int dev;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_E_CUDA;
@@ -597,14 +662,14 @@ extern "C" unsigned long long attn_launch_count(void) {
 
 #ifdef ATTN_DEBUG_CHECKS
 // Debug builds only: from now on, the MMA issuer of block (0, 0, 0) of
-// `kernel` (1 forward, 2 backward main, 3 deterministic dQ, 4 fp8 forward)
-// lets its wait at iteration `iteration` run out; kernel <= 0 clears it.
+// `kernel` (1 forward, 2 backward main, 3 deterministic dQ, 4 fp8 forward,
+// 5 score recompute) lets its wait at iteration `iteration` run out; kernel <= 0 clears it.
 extern "C" int attn_debug_inject_stall(int kernel, int iteration) {
     if (kernel <= 0) {
         g_debug_stall.store(-1);
         return ATTN_OK;
     }
-    if (kernel > 4 || iteration < 0 || iteration > 0xffff) return ATTN_E_ARG;
+    if (kernel > 5 || iteration < 0 || iteration > 0xffff) return ATTN_E_ARG;
     g_debug_stall.store((kernel << 16) | iteration);
     return ATTN_OK;
 }

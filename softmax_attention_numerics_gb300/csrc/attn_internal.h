@@ -63,6 +63,14 @@ struct Problem {
     int lazy;           // 1: lazy rescale with threshold 8 (log2 units)
     int* err;           // device error word
     int debug_stall;    // debug builds: (kernel << 16 | iteration) whose wait runs out; -1 none
+
+    // score recompute: score [rows, sc_w] fp32 (rows = B*Sq dense, T varlen),
+    // l1 [rows], l1_part [key tiles][l1_rows] workspace
+    float* score;
+    float* l1;
+    float* l1_part;
+    int64_t sc_w;
+    int64_t l1_rows;
 };
 
 // Error codes written to the device error word (match include/attn_gb300.h).
@@ -120,6 +128,8 @@ cudaError_t launch_bwd_main(const Problem& p, bool with_dq_atomics, cudaStream_t
 cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_deterministic(const Problem& p, cudaStream_t stream);
 cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream);
+cudaError_t launch_score_recompute(const Problem& p, cudaStream_t stream);
+int score_key_tiles(int64_t width);
 cudaError_t launch_zero_trailing_bwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_fp8_transpose_v(const Fp8Problem& p, cudaStream_t stream);
 cudaError_t launch_fwd_fp8(const Fp8Problem& p, cudaStream_t stream);

@@ -127,6 +127,48 @@ def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, causal=False, scale=N
     return out, lse
 
 
+def score_workspace_bytes(q, k, cu_seqlens=None, max_seqlen=None):
+    lib = _lib.load()
+    msl = _max_seqlen(cu_seqlens, max_seqlen)
+    descs = [tensor_desc(x) for x in (q, k, cu_seqlens)]
+    return int(lib.attn_score_workspace_bytes(*[_ref(d) for d in descs], msl))
+
+
+def attn_score_recompute(q, k, lse, cu_seqlens=None, max_seqlen=None, causal=False, scale=None,
+                         score=None, l1=None, workspace=None, stream=None):
+    """Attention targets recomputed from the forward's lse, summed over the
+    query heads, and each row's L1 norm.  Returns (score, l1), both fp32.
+
+    Dense: q [B,Sq,Hq,D], k [B,Sk,Hkv,D], lse [B,Hq,Sq] -> score [B,Sq,Sk],
+    l1 [B,Sq].  Varlen: q [T,Hq,D], k [T,Hkv,D], lse [Hq,T] -> score
+    [T,max_seqlen], l1 [T].  scale=None means 1/sqrt(D).
+    """
+    lib = _lib.load()
+    s = _stream(stream, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    msl = _max_seqlen(cu_seqlens, max_seqlen)
+    with torch.cuda.device(q.device), torch.cuda.stream(s):
+        if cu_seqlens is None:
+            sshape, lshape = (q.shape[0], q.shape[1], k.shape[1]), (q.shape[0], q.shape[1])
+        else:
+            sshape, lshape = (q.shape[0], msl), (q.shape[0],)
+        if score is None:
+            score = torch.empty(sshape, dtype=torch.float32, device=q.device)
+        if l1 is None:
+            l1 = torch.empty(lshape, dtype=torch.float32, device=q.device)
+        nbytes = score_workspace_bytes(q, k, cu_seqlens, msl)
+        if workspace is None or workspace.numel() < nbytes:
+            workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+        descs = [tensor_desc(x) for x in (q, k, lse, cu_seqlens, score, l1)]
+        rc = lib.attn_score_recompute(*[_ref(d) for d in descs[:4]], msl, 1 if causal else 0,
+                                      float(scale), _ref(descs[4]), _ref(descs[5]),
+                                      ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), 0,
+                                      ctypes.c_void_p(s.cuda_stream))
+    _lib.check(rc, "attn_score_recompute")
+    return score, l1
+
+
 def bwd_workspace_bytes(q, k, deterministic=False):
     lib = _lib.load()
     dq_, dk_ = tensor_desc(q), tensor_desc(k)

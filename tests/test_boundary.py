@@ -322,6 +322,47 @@ def test_fp8_forward_contract(lib):
     assert call_fwd_fp8(lib, fp8_dense(), ws=FAKE + 16, ws_bytes=n) == E["ATTN_E_WORKSPACE"]
 
 
+# ---------------------------------------------------------------- score recompute
+
+def call_score(lib, t, score, l1, cu=None, max_seqlen=0, ws=FAKE, ws_bytes=1 << 40, flags=0):
+    return lib.attn_score_recompute(R(t["q"]), R(t["k"]), R(t["lse"]), R(cu), max_seqlen, 0, 0.1,
+                                    R(score), R(l1), ctypes.c_void_p(ws), ws_bytes, flags, None)
+
+
+def test_score_recompute_contract(lib):
+    """The score recompute takes attn_fwd's q, k and lse (PFCCLab PR #9,
+    section 3) and writes fp32 [B,Sq,Sk] scores and [B,Sq] L1 norms; every
+    malformed call is rejected before a launch."""
+    t = dense()
+    sc, l1 = desc([2, 100, 77], _lib.ATTN_F32), desc([2, 100], _lib.ATTN_F32)
+    stop = (E["ATTN_E_DEVICE"], E["ATTN_E_CUDA"])
+    assert call_score(lib, t, sc, l1) in stop                      # valid: stops at the device
+    assert call_score(lib, t, sc, l1, flags=1) == E["ATTN_E_ARG"]
+    assert call_score(lib, t, desc([2, 100, 77]), l1) == E["ATTN_E_DTYPE"]         # bf16 score
+    assert call_score(lib, t, desc([2, 77, 100], _lib.ATTN_F32), l1) == E["ATTN_E_SHAPE"]
+    assert call_score(lib, t, sc, desc([100, 2], _lib.ATTN_F32)) == E["ATTN_E_SHAPE"]
+    t2 = dense()
+    t2["lse"] = desc([2, 100, 4], _lib.ATTN_F32)                     # transposed lse
+    assert call_score(lib, t2, sc, l1) == E["ATTN_E_SHAPE"]
+    assert call_score(lib, dense(D=96), sc, l1) == E["ATTN_E_UNSUPPORTED"]
+    strided = desc([2, 100, 77], _lib.ATTN_F32, stride=[100 * 80, 80, 1])
+    assert call_score(lib, t, strided, l1) == E["ATTN_E_LAYOUT"]
+    n = lib.attn_score_workspace_bytes(R(t["q"]), R(t["k"]), None, 0)
+    assert n == -(-1 * 200 * 4 // 256) * 256                        # one key tile x 200 rows
+    assert call_score(lib, t, sc, l1, ws_bytes=n - 1) == E["ATTN_E_WORKSPACE"]
+    assert call_score(lib, t, sc, l1, ws=FAKE + 16, ws_bytes=n) == E["ATTN_E_WORKSPACE"]
+    # varlen: score [T, max_seqlen], l1 [T]
+    T = 300
+    tv = dict(q=desc([T, 4, 64]), k=desc([T, 2, 64]), lse=desc([4, T], _lib.ATTN_F32))
+    cu = desc([4], _lib.ATTN_I32)
+    assert call_score(lib, tv, desc([T, 130], _lib.ATTN_F32), desc([T], _lib.ATTN_F32), cu=cu,
+                      max_seqlen=130) in stop
+    assert call_score(lib, tv, desc([T, 129], _lib.ATTN_F32), desc([T], _lib.ATTN_F32), cu=cu,
+                      max_seqlen=130) == E["ATTN_E_SHAPE"]
+    assert lib.attn_score_workspace_bytes(R(tv["q"]), R(tv["k"]), R(cu), 130) == \
+        -(-2 * T * 4 // 256) * 256                                  # two key tiles
+
+
 def test_poisoned_staging_variant_builds_and_exports_the_abi():
     """The race-check debug library (ATTN_POISON_SMEM) compiles for sm_103a
     from the same sources and exports the same C ABI."""
@@ -354,7 +395,7 @@ def test_checked_variant_builds_and_exports_the_abi_and_the_stall_hook():
     fn = dbg.attn_debug_inject_stall
     fn.restype = ctypes.c_int
     fn.argtypes = [ctypes.c_int, ctypes.c_int]
-    assert fn(5, 0) == E["ATTN_E_ARG"]
+    assert fn(6, 0) == E["ATTN_E_ARG"]
     assert fn(1, -1) == E["ATTN_E_ARG"]
     assert fn(2, 70000) == E["ATTN_E_ARG"]
     assert fn(2, 3) == 0
