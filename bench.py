@@ -50,6 +50,10 @@ def parse(argv=None):
                          "forward alone (bf16 out)")
     ap.add_argument("--deterministic", action="store_true",
                     help="dQ by the per-query-tile kernel instead of fp32 reductions")
+    ap.add_argument("--workload", default="attention", choices=["attention", "score"],
+                    help="score: the head-summed score recompute (its own metric and line)")
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="kv heads of the score workload (0: 1, all q heads share it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-oracle-reps", type=int, default=1, help=argparse.SUPPRESS)
@@ -411,6 +415,111 @@ def run_fp8_forward(a):
     print(json.dumps(line))
 
 
+# ---------------------------------------------------------------- score recompute
+
+def run_score(a):
+    """--workload score: attention targets recomputed from the forward's lse
+    and summed over the query heads, with the L1 norm of every row.  One step =
+    attn_score_recompute (the tile kernel and its L1 reduction) on a resident
+    q, k and lse.  Work: 2 D flop per (query, key, head) on the tensor cores
+    (halved when causal) and one exp2 per term; the fp32 score is written once."""
+    import torch
+    from softmax_attention_numerics_gb300 import _lib, attn_fwd, attn_score_recompute
+    from softmax_attention_numerics_gb300 import build as _build
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    lib = _lib.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B, H, S, D = 1, a.heads, a.seqlen, a.head_dim
+    Hkv = a.kv_heads if a.kv_heads > 0 else 1
+    g = torch.Generator(device=dev).manual_seed(42)
+    q = torch.randn(B, S, H, D, generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn(B, S, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+    _, lse = attn_fwd(q, k, k, causal=a.causal)
+    score = torch.empty(B, S, S, dtype=torch.float32, device=dev)
+    l1 = torch.empty(B, S, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        attn_score_recompute(q, k, lse, causal=a.causal, score=score, l1=l1, stream=stream)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(a.steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in ev:
+            e0.record(stream)
+            e1.record(stream)
+        for _ in range(a.warmup):
+            step()
+    stream.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = lib.attn_launch_count()
+    with ClockSampler(0) as clk:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(a.steps):
+                lib.attn_profile_events(_lib.ATTN_STAGE_SCORE, ctypes_ptr(ev[i][0]),
+                                        ctypes_ptr(ev[i][1]))
+                step()
+            t1.record(stream)
+        lib.attn_profile_events(_lib.ATTN_STAGE_SCORE, None, None)
+        stream.synchronize()
+    launches = lib.attn_launch_count() - launches0
+    ms = t0.elapsed_time(t1)
+    flops = 2.0 * B * S * S * H * D / (2 if a.causal else 1)
+    value = flops * a.steps / (ms / 1e3) / 1e12
+    kern_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    achieved = flops / (kern_ms / 1e3) / 1e12
+    peaks, kind = measured_peaks()
+    peak = peaks.get("bf16_tflops", 1900.0)
+    out_bytes = 4.0 * B * S * S
+    nonfinite = int((~torch.isfinite(score)).sum()) + int((~torch.isfinite(l1)).sum())
+    l1_err = float((l1 - H).abs().max())
+    # e2e: q, k, lse from pinned host memory in, score and l1 back, every step
+    host_in = [t.cpu().pin_memory() for t in (q, k, lse)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (score, l1)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e_steps = max(1, min(a.steps, 3))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e_steps):
+            for dst, src in zip((q, k, lse), host_in):
+                dst.copy_(src, non_blocking=True)
+            step()
+            for dst, src in zip(host_out, (score, l1)):
+                dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    line = {
+        "metric": "attention score recompute TFLOP/s (head-summed exp2 targets + L1 norm)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "score_recompute B=%d Hq=%d Hkv=%d S=%d D=%d %s" % (
+                       B, H, Hkv, S, D, "causal" if a.causal else "non-causal"),
+                   "B": B, "Hq": H, "Hkv": Hkv, "S": S, "D": D, "causal": a.causal,
+                   "parallelism": "single",
+                   "l2": "no flush: the fp32 score (%d MiB) exceeds L2" % (out_bytes / 2 ** 20)},
+        "roofline": {"bound": "tensor", "kernel": "score_sm100", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": "%s bf16_tflops" % kind,
+                     "score_write_gbs": out_bytes / (kern_ms / 1e3) / 1e9},
+        "cpu_baseline": None,
+        "e2e": {"value": flops * e_steps / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "extra": {"kernel_ms": kern_ms, "nonfinite_outputs": nonfinite,
+                  "l1_max_abs_err_vs_head_count": l1_err},
+    }
+    print(json.dumps(line))
+
+
 # ---------------------------------------------------------------- our arm
 
 def main():
@@ -420,6 +529,11 @@ def main():
         return
     if a.impl == "reference":
         run_reference(a)
+        return
+    if a.workload == "score":
+        if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+            raise SystemExit("--workload score: one GPU")
+        run_score(a)
         return
     if a.dtype == "e4m3":
         if a.head_dim != 128 or a.deterministic or int(os.environ.get("WORLD_SIZE", "1")) > 1:

@@ -13,17 +13,17 @@
 //
 // One CTA = a 128 x 128 (query, key) tile of one batch / sequence; it loops
 // over the query heads:
-//   warp 8   TMA producer: Q_h tiles through a 2-stage ring, the K tile of
-//            each kv head through another (q heads of a GQA group share it)
+//   warp 8   TMA producer: Q_h tiles through a 4-stage ring, the K tile of
+//            each kv head through a 2-stage one (q heads of a GQA group share it)
 //   warp 9   TMEM allocator and single-thread UMMA issuer: S_h = Q_h K^T into
 //            TMEM buffer h & 1
-//   warps 0-3 / 4-7  even / odd heads: thread = query row = TMEM lane, the
-//            128 terms of its row accumulated in registers
-// The two warpgroups then add their sums through shared memory, and all
-// eight warps store the fp32 tile with full-row coalesced stores (rows past
-// the sequence are never written).  Each CTA writes its rows' partial L1
-// norm for this key tile; l1_reduce_kernel adds the partials of a row in
-// key-tile order, so both outputs are bit-reproducible.
+//   warps 0-3 / 4-7  key columns 0-63 / 64-127 of every head: thread = query
+//            row = TMEM lane, its 64 terms accumulated in registers; one
+//            TMEM load per head, and both warpgroups release the buffer
+// Each thread stores its row's 64 sums from registers (rows past the sequence
+// are never written).  Each CTA writes its rows' partial L1 norm for this key
+// tile; l1_reduce_kernel adds the partials of a row in key-tile order, so both
+// outputs are bit-reproducible.
 #include "sm100_ptx.cuh"
 
 namespace attn {
@@ -34,19 +34,20 @@ using namespace sm100;
 constexpr int kScThreads = 320;
 constexpr int kSt = 128;                 // query and key tile
 constexpr float kScoreClamp = 120.0f;    // log2 units
-constexpr int kStagePitch = kSt + 4;     // fp32 words per staging row (bank spread)
 
 template <int D>
 struct ScLayout {
     static constexpr int kBlocks = D / 64;
     static constexpr int kTileBytes = kSt * D * 2;
-    static constexpr int kQ = 0;                         // 2 stages
-    static constexpr int kK = 2 * kTileBytes;            // 2 stages
-    static constexpr int kStage = 4 * kTileBytes;        // fp32 [128][kStagePitch]
-    static constexpr int kBar = kStage + kSt * kStagePitch * 4;
-    static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKFull = 4, kBarKEmpty = 6;
-    static constexpr int kBarSFull = 8, kBarSFree = 10, kBarDrain = 12;
-    static constexpr int kNumBars = 13;
+    static constexpr int kQStages = 4;                   // a Q_h tile per head: keep loads ahead
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQStages * kTileBytes;     // 2 stages
+    static constexpr int kHalf = kK + 2 * kTileBytes;    // fp32 [128]: odd half-row sums
+    static constexpr int kBar = kHalf + kSt * 4;
+    static constexpr int kBarQFull = 0, kBarQEmpty = kQStages, kBarKFull = 2 * kQStages;
+    static constexpr int kBarKEmpty = kBarKFull + 2, kBarSFull = kBarKEmpty + 2;
+    static constexpr int kBarSFree = kBarSFull + 2, kBarDrain = kBarSFree + 2;
+    static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16 + 1024;     // + alignment slack
     static constexpr uint32_t kTmemCols = 256;
@@ -56,11 +57,11 @@ struct ScoreMaps {
     CUtensorMap q, k;
 };
 
-// Rows [m0, m0 + 128) x columns [n0, n0 + 128) of the score tile from the
-// shared staging tile (or zeros when stage == nullptr); warp w writes rows
-// 16w .. 16w + 15, lane l columns 4l .. 4l + 3.
-__device__ __forceinline__ void store_tile(const Problem& p, const float* stage, int b, int row_base,
-                                           int m0, int n0, int len_q, int warp, int lane) {
+// Zeros for rows [m0, m0 + 128) x columns [n0, n0 + 128) of the score (a tile
+// with no visible pair); warp w writes rows 16w .. 16w + 15, lane l columns
+// 4l .. 4l + 3.
+__device__ __forceinline__ void store_zero_tile(const Problem& p, int b, int row_base, int m0, int n0,
+                                                int len_q, int warp, int lane) {
     const int64_t W = p.sc_w;
     const int64_t rb = p.varlen ? row_base : static_cast<int64_t>(b) * p.Sq;
     for (int rr = 0; rr < 16; ++rr) {
@@ -68,15 +69,12 @@ __device__ __forceinline__ void store_tile(const Problem& p, const float* stage,
         if (m0 + row >= len_q) break;
         float* dst = p.score + (rb + m0 + row) * W;
         const int c0 = n0 + 4 * lane;
-        float v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = stage ? stage[row * kStagePitch + 4 * lane + u] : 0.f;
         if (c0 + 3 < W && (W & 3) == 0) {
-            *reinterpret_cast<float4*>(dst + c0) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(dst + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (c0 + u < W) dst[c0 + u] = v[u];
+                if (c0 + u < W) dst[c0 + u] = 0.f;
         }
     }
 }
@@ -92,7 +90,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
     auto bar = [&](int i) { return sbase + L::kBar + 8u * i; };
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
-    float* stage = reinterpret_cast<float*>(smem + L::kStage);
+    float* half_sum = reinterpret_cast<float*>(smem + L::kHalf);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z;
@@ -108,14 +106,14 @@ __global__ void __launch_bounds__(kScThreads, 1)
     // A tile with no visible pair (keys past the sequence, or wholly above
     // the causal diagonal) is written as zeros.
     if (n0 >= si.len_k || (p.causal && n0 > m0 + kSt - 1)) {
-        if (warp < 8) store_tile(p, nullptr, b, row_base, m0, n0, si.len_q, warp, lane);
+        if (warp < 8) store_zero_tile(p, b, row_base, m0, n0, si.len_q, warp, lane);
         for (int r = tid; r < nrow; r += kScThreads) part[r] = 0.f;
         return;
     }
 
     if (tid == 0) {
         for (int i = 0; i < L::kNumBars; ++i)
-            mbar_init(bar(i), (i == L::kBarSFree || i == L::kBarSFree + 1) ? 128 : 1);
+            mbar_init(bar(i), (i == L::kBarSFree || i == L::kBarSFree + 1) ? 256 : 1);
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -148,8 +146,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
                                     row_base + n0, bcoord, bar(L::kBarKFull + ks));
                     k_issued = kv + 1;
                 }
-                const int s = h & 1;
-                if (!mbar_wait(bar(L::kBarQEmpty + s), ((h >> 1) & 1) ^ 1, abort_flag)) break;
+                const int s = h % L::kQStages, qr = h / L::kQStages;
+                if (!mbar_wait(bar(L::kBarQEmpty + s), (qr & 1) ^ 1, abort_flag)) break;
                 mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kBlocks; ++c)
@@ -160,8 +158,9 @@ __global__ void __launch_bounds__(kScThreads, 1)
             if (*abort_flag) {
                 // Let the copies in flight land before the CTA exits.
                 volatile int no_abort = 0;
-                for (int h = max(0, q_issued - 2); h < q_issued; ++h)
-                    mbar_wait(bar(L::kBarQFull + (h & 1)), (h >> 1) & 1, &no_abort, kDrainBudgetNs);
+                for (int h = max(0, q_issued - L::kQStages); h < q_issued; ++h)
+                    mbar_wait(bar(L::kBarQFull + h % L::kQStages), (h / L::kQStages) & 1, &no_abort,
+                              kDrainBudgetNs);
                 for (int kv = max(0, k_issued - 2); kv < k_issued; ++kv)
                     mbar_wait(bar(L::kBarKFull + (kv & 1)), (kv >> 1) & 1, &no_abort, kDrainBudgetNs);
             }
@@ -174,10 +173,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
             bool ok = true;
             for (int h = 0; ok && h < H; ++h) {
                 if (!(ok = dbg_stall(p.debug_stall, kStallScore, h, bar(L::kBarDrain), abort_flag))) break;
-                const int s = h & 1, kv = h / G, ks = kv & 1, buf = h & 1;
-                if (!(ok = mbar_wait(bar(L::kBarQFull + s), (h >> 1) & 1, abort_flag))) break;
+                const int s = h % L::kQStages, kv = h / G, ks = kv & 1, buf = h & 1;
+                if (!(ok = mbar_wait(bar(L::kBarQFull + s), (h / L::kQStages) & 1, abort_flag))) break;
                 if (!(ok = mbar_wait(bar(L::kBarKFull + ks), (kv >> 1) & 1, abort_flag))) break;
-                // buffer `buf` is free once its warpgroup has read head h - 2
+                // buffer `buf` is free once both warpgroups have read head h - 2
                 if (h >= 2 && !(ok = mbar_wait(bar(L::kBarSFree + buf), ((h >> 1) - 1) & 1, abort_flag)))
                     break;
                 tc_fence_after();
@@ -205,72 +204,68 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const int row = wq * 32 + lane;
         const int i = m0 + row;                              // query row in the sequence
         const bool row_in = i < si.len_q;
-        const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + 128 * wg;
+        const int c0 = 64 * wg;                              // this warpgroup's key columns
+        const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + c0;
         const int jmax = p.causal ? min(si.len_k, i + 1) : si.len_k;   // keys < jmax visible
-        const bool full = n0 + kSt <= jmax;                  // every key of the tile visible
+        const bool full = n0 + c0 + 64 <= jmax;              // every key of the half visible
         const float c = p.scale_log2;
         const int64_t lse_row = b * p.lse_b + row_base + i;
-        float acc[kSt];
+        float acc[64];
 #pragma unroll
-        for (int e = 0; e < kSt; ++e) acc[e] = 0.f;
+        for (int e = 0; e < 64; ++e) acc[e] = 0.f;
         bool ok = true;
-        float nl_next = (row_in && wg < H) ? -p.lse[lse_row + wg * p.lse_h] * kLog2e : 0.f;
-        for (int h = wg; h < H; h += 2) {
+        float nl_next = row_in ? -p.lse[lse_row] * kLog2e : 0.f;
+        for (int h = 0; h < H; ++h) {
             const float nl = nl_next;                        // -lse2 of (row, h)
-            if (h + 2 < H) nl_next = row_in ? -p.lse[lse_row + (h + 2) * p.lse_h] * kLog2e : 0.f;
-            ok = mbar_wait(bar(L::kBarSFull + wg), (h >> 1) & 1, abort_flag);
+            if (h + 1 < H) nl_next = row_in ? -p.lse[lse_row + (h + 1) * p.lse_h] * kLog2e : 0.f;
+            const int buf = h & 1;
+            ok = mbar_wait(bar(L::kBarSFull + buf), (h >> 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            uint32_t v[64];
+            tmem_ld32x2(tS + 128 * buf, v, tS + 128 * buf + 32, v + 32);
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarSFree + buf));            // the values are in registers
+            if (full && row_in) {
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                uint32_t v[16];
-                tmem_ld16(tS + 16 * cc, v);
-                if (full && row_in) {
+                for (int e = 0; e < 64; ++e)
+                    acc[e] += ex2(fminf(fmaf(__uint_as_float(v[e]), c, nl), kScoreClamp));
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        acc[16 * cc + e] += ex2(fminf(fmaf(__uint_as_float(v[e]), c, nl), kScoreClamp));
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const bool vis = row_in && n0 + 16 * cc + e < jmax;
-                        const float t = ex2(fminf(fmaf(__uint_as_float(v[e]), c, nl), kScoreClamp));
-                        acc[16 * cc + e] += vis ? t : 0.f;
-                    }
+                for (int e = 0; e < 64; ++e) {
+                    const bool vis = row_in && n0 + c0 + e < jmax;
+                    const float t = ex2(fminf(fmaf(__uint_as_float(v[e]), c, nl), kScoreClamp));
+                    acc[e] += vis ? t : 0.f;
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar(L::kBarSFree + wg));
         }
-        // The odd-head sums go through shared memory; the even-head warpgroup
-        // adds them to its own, writes the row's partial L1 norm, and leaves
-        // the total in the staging tile for the stores below.
-        if (wg == 1 && ok) {
-            float* dst = stage + row * kStagePitch;
+        // Each thread stores its row's 64 sums directly (full 16-byte vectors
+        // where the row stride allows); warpgroup 1 leaves its half-row sum in
+        // shared memory and warpgroup 0 adds it to its own: the row's partial
+        // L1 norm for this key tile, in a fixed order.
+        float hs = 0.f;
 #pragma unroll
-            for (int e = 0; e < kSt; e += 4)
-                *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-        }
-        named_bar_sync(1, 256);
-        if (wg == 0 && ok) {
-            float* dst = stage + row * kStagePitch;
-            float sum = 0.f;
+        for (int e = 0; e < 64; e += 4) hs += (acc[e] + acc[e + 1]) + (acc[e + 2] + acc[e + 3]);
+        if (wg == 1) half_sum[row] = hs;
+        if (ok && row_in) {
+            const int64_t W = p.sc_w;
+            const int64_t rb = p.varlen ? row_base : static_cast<int64_t>(b) * p.Sq;
+            float* dst = p.score + (rb + i) * W + n0 + c0;
+            if (n0 + c0 + 63 < W && (W & 3) == 0) {
 #pragma unroll
-            for (int e = 0; e < kSt; e += 4) {
-                float4 o = *reinterpret_cast<const float4*>(dst + e);   // odd heads (0 if H = 1)
-                o.x += acc[e];
-                o.y += acc[e + 1];
-                o.z += acc[e + 2];
-                o.w += acc[e + 3];
-                sum += (o.x + o.y) + (o.z + o.w);
-                *reinterpret_cast<float4*>(dst + e) = o;
+                for (int e = 0; e < 64; e += 4)
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 64; ++e)
+                    if (n0 + c0 + e < W) dst[e] = acc[e];
             }
-            if (row_in) part[row] = sum;
         }
         named_bar_sync(1, 256);
-        if (ok) store_tile(p, stage, b, row_base, m0, n0, si.len_q, warp, lane);
+        if (wg == 0 && ok && row_in) part[row] = hs + half_sum[row];
     }
 
     tc_fence_before();

@@ -78,15 +78,34 @@ def test_checked_build_fp8_forward_matches_product_build(checked_lib):
         assert torch.equal(a, b)
 
 
+def test_checked_build_score_recompute_matches_product_build(checked_lib):
+    from softmax_attention_numerics_gb300 import _lib, attn_fwd, attn_score_recompute, get_error
+    q, k, _, _ = (t.cuda() for t in W.dense_qkvdo(2, 300, 300, 8, 2, 128, seed=34))
+    _, lse = attn_fwd(q, k, k, causal=True)
+    ref = attn_score_recompute(q, k, lse, causal=True)
+    with _lib.use_library(checked_lib):
+        got = attn_score_recompute(q, k, lse, causal=True)
+        torch.cuda.synchronize()
+        assert get_error() == 0
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+
+
 # (kernel, iteration of its MMA issuer's loop): 1 forward, 2 backward main,
-# 3 deterministic dQ, 4 fp8 forward.
-STALLS = [(1, 0), (1, 3), (2, 0), (2, 5), (3, 0), (3, 2), (4, 0), (4, 2)]
+# 3 deterministic dQ, 4 fp8 forward, 5 score recompute (the loop runs over heads).
+STALLS = [(1, 0), (1, 3), (2, 0), (2, 5), (3, 0), (3, 2), (4, 0), (4, 2), (5, 0), (5, 3)]
 
 
 def _stalled_call(kernel):
     """The call whose kernel the stall targets, on a problem where block
     (0, 0, 0) runs more than three iterations of its loop."""
     from softmax_attention_numerics_gb300 import attn_bwd, attn_fwd, attn_fwd_fp8
+    from softmax_attention_numerics_gb300 import attn_score_recompute
+    if kernel == 5:
+        q, k, _, _ = (t.cuda() for t in W.dense_qkvdo(1, 300, 300, 8, 2, 128, seed=35))
+        lse = torch.zeros(1, 8, 300, device="cuda")
+        attn_score_recompute(q, k, lse)
+        return
     if kernel == 4:
         c = W.fp8_qkv(B=1, S=700, H=2, D=128, k_scale=1.0, v="randn", seed=9)
         q, k, v = (c[n].cuda().view(torch.float8_e4m3fn) for n in ("q", "k", "v"))
