@@ -32,6 +32,12 @@ Workloads (sizes and value distributions as the pages give them):
   B=1, H=16, S=12288, D=128 (FlyDSL PR #1033, "The fp8 helper, second
   commit"); each tensor is divided by amax/448 and rounded to E4M3 by
   PyTorch's float8 conversion.
+* ``dsa_case``       sparse top-k attention with a sink (NVIDIA/cudnn-frontend
+  PR #429: S = 512 queries, S_kv = 2048 kv rows, H = 64, D = 576 with values
+  in the first 512 columns, or D = 512, top-k = 128, with and without
+  topk_length): q, kv, dout = N(0,1); every token lists K distinct kv rows
+  drawn uniformly; with ``length`` each token's topk_length is uniform in
+  [1, K] and the entries past it are -1; the sink per head is N(0,1).
 """
 from __future__ import annotations
 
@@ -182,3 +188,24 @@ def fp8_qkv(B=1, S=12288, H=16, D=128, k_scale=1000.0, v="ones", causal=False, s
     (qc, dq), (kc, dk), (vc, dv) = _to_e4m3(q), _to_e4m3(k), _to_e4m3(vv)
     return dict(q=qc, k=kc, v=vc, descale_q=dq, descale_k=dk, descale_v=dv, causal=causal,
                 scale=1.0 / math.sqrt(D))
+
+
+def dsa_case(B=1, S=512, Skv=2048, H=64, D=576, K=128, sink=True, length=True, seed=42,
+             dtype=BF16):
+    """Inputs of the sparse top-k backward (the forward's out and lse come
+    from whichever side runs it).  Returns q [B,S,H,D], kv [B,Skv,D], dout
+    [B,S,H,512] (16-bit), topk_idxs int32 [B,S,K], topk_length int32 [B,S]
+    or None, attn_sink fp32 [H] or None."""
+    g = _gen(seed)
+    q = _randn(g, (B, S, H, D)).to(dtype)
+    kv = _randn(g, (B, Skv, D)).to(dtype)
+    dout = _randn(g, (B, S, H, 512)).to(dtype)
+    keys = torch.rand(B, S, Skv, generator=g)
+    idx = keys.argsort(dim=2)[:, :, :K].to(torch.int32)       # K distinct rows per token
+    ln = None
+    if length:
+        ln = torch.randint(1, K + 1, (B, S), generator=g, dtype=torch.int32)
+        pos = torch.arange(K, dtype=torch.int32)
+        idx = torch.where(pos[None, None, :] < ln[:, :, None], idx, torch.full_like(idx, -1))
+    sk = _randn(g, (H,)) if sink else None
+    return dict(q=q, kv=kv, dout=dout, topk_idxs=idx.contiguous(), topk_length=ln, attn_sink=sk)

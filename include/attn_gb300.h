@@ -300,6 +300,61 @@ size_t attn_score_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* k
                                   const attn_tensor_t* cu_seqlens, int32_t max_seqlen);
 
 /*
+ * attn_sparse_bwd - backward of sparse top-k attention with an attention sink
+ * (the DSA backward).  NVIDIA/cudnn-frontend PR #429 fixes the interface
+ * (inputs q, kv, out, dout, lse, attn_sink, topk_idxs, optional topk_length;
+ * outputs dq, dkv, d_sink; head dim 512, or 576 in the MLA form whose values
+ * are the first 512 columns of the kv rows), the shape contract checked
+ * against q before launch, the zero-fills on the launch stream and a real
+ * fp16 path.  The page prints no formula; the library computes, for token i
+ * of batch b and its listed kv rows k_e (v_e = k_e[:512]):
+ *
+ *   P_he = exp(scale q_h . k_e - lse_h),   Delta_h = dout_h . out_h,
+ *   dS_he = P_he (dout_h . v_e - Delta_h),
+ *   dq_h = scale sum_e dS_he k_e,
+ *   dkv[b, idx_e] += scale sum_h dS_he q_h  (+ sum_h P_he dout_h on the
+ *                                             first 512 columns),
+ *   d_sink[h] = - sum over all tokens of exp(attn_sink[h] - lse_h) Delta_h.
+ *
+ *   q            [B, S, H, Dqk] bf16 or fp16, H = 64, Dqk = 512 or 576
+ *   kv           [B, S_kv, Dqk] q's type: one row set shared by the heads
+ *   out, dout    [B, S, H, 512] q's type (out: the forward's output)
+ *   lse          [B, S, H] fp32, contiguous: log of each (token, head)'s
+ *                softmax normaliser, exp(attn_sink[h]) included (natural log)
+ *   attn_sink    [H] fp32 contiguous, or NULL (no sink)
+ *   topk_idxs    [B, S, K] int32 contiguous, K >= 0: kv rows of each token.
+ *                Entry e takes part when e < topk_length[b, i] and
+ *                0 <= idx < S_kv; other entries (e.g. -1 padding) are
+ *                ignored.  Repeated rows count once per entry.
+ *   topk_length  [B, S] int32 contiguous, or NULL (all K entries)
+ *   scale        finite
+ *   dq, dkv      q's / kv's shape and type, contiguous; written (not
+ *                accumulated into).  A token with no valid entry gets dq = 0.
+ *   d_sink       [H] fp32, written; given exactly when attn_sink is
+ *   workspace    attn_sparse_bwd_workspace_bytes(q, kv, attn_sink != NULL)
+ *                bytes, 256-byte aligned (fp32 dkv accumulator, Delta and the
+ *                sink terms)
+ *   flags        0
+ * dq and d_sink are bitwise reproducible; dkv is the 16-bit rounding of fp32
+ * sums whose order varies from run to run.  Returns ATTN_E_UNSUPPORTED for
+ * H != 64 or Dqk not in {512, 576}, ATTN_E_SHAPE / ATTN_E_DTYPE /
+ * ATTN_E_LAYOUT / ATTN_E_DEVICE for any tensor off the contract, ATTN_E_ARG
+ * for a missing tensor, a non-finite scale, nonzero flags or a sink without
+ * d_sink (or the reverse).
+ */
+int attn_sparse_bwd(const attn_tensor_t* q, const attn_tensor_t* kv, const attn_tensor_t* out,
+                    const attn_tensor_t* dout, const attn_tensor_t* lse,
+                    const attn_tensor_t* attn_sink, const attn_tensor_t* topk_idxs,
+                    const attn_tensor_t* topk_length, float scale, attn_tensor_t* dq,
+                    attn_tensor_t* dkv, attn_tensor_t* d_sink, void* workspace,
+                    size_t workspace_bytes, uint32_t flags, attn_stream_t stream);
+
+/* attn_sparse_bwd_workspace_bytes - workspace attn_sparse_bwd needs (0 if q
+ * or kv break the contract); with_sink: nonzero when attn_sink is given. */
+size_t attn_sparse_bwd_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* kv,
+                                       int with_sink);
+
+/*
  * attn_get_error - synchronises `stream`, then returns and clears the error
  * word of the current device: ATTN_OK, ATTN_E_SEQLENS, ATTN_E_TIMEOUT or
  * ATTN_E_INTERNAL
@@ -343,7 +398,8 @@ int attn_selftest_wait_timeout(uint32_t budget_us, attn_stream_t stream);
  * skip the access instead of trapping, and exports one more function,
  * int attn_debug_inject_stall(int kernel, int iteration): from then on the
  * MMA issuer of block (0, 0, 0) of `kernel` (1 forward, 2 backward main,
- * 3 deterministic dQ, 4 fp8 forward, 5 score recompute) lets its wait at loop iteration
+ * 3 deterministic dQ, 4 fp8 forward, 5 score recompute, 6 sparse backward, whose
+ * loop runs over work items) lets its wait at loop iteration
  * `iteration` (0 .. 65535) run out after 200 us, so that the kernel unwinds
  * and reports ATTN_E_TIMEOUT; kernel <= 0 turns it off; ATTN_E_ARG for
  * arguments out of range.
@@ -364,7 +420,8 @@ enum {
     ATTN_STAGE_BWD_MAIN = 2,       /* dK, dV (and atomic dQ partials)        */
     ATTN_STAGE_BWD_DQ = 3,         /* dQ convert, or the deterministic dQ    */
     ATTN_STAGE_SCORE = 4,          /* score recompute (then its L1 reduce)   */
-    ATTN_STAGE_COUNT = 5
+    ATTN_STAGE_SPARSE = 5,         /* sparse top-k backward main kernel      */
+    ATTN_STAGE_COUNT = 6
 };
 int attn_profile_events(int stage, void* before, void* after);
 

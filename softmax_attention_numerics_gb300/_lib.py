@@ -19,12 +19,14 @@ ERRORS = {
 
 # Every symbol the header declares.
 EXPORTS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_fp8_workspace_bytes", "attn_score_recompute",
-           "attn_score_workspace_bytes", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_bytes", "attn_get_error",
+           "attn_score_workspace_bytes", "attn_sparse_bwd", "attn_sparse_bwd_workspace_bytes",
+           "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_bytes", "attn_get_error",
            "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_profile_events",
            "attn_launch_count", "attn_selftest_wait_timeout")
 
 ATTN_STAGE_FWD, ATTN_STAGE_BWD_PREPROCESS, ATTN_STAGE_BWD_MAIN, ATTN_STAGE_BWD_DQ = 0, 1, 2, 3
 ATTN_STAGE_SCORE = 4
+ATTN_STAGE_SPARSE = 5
 
 
 class AttnTensor(ctypes.Structure):
@@ -91,6 +93,12 @@ def load_path(path):
                                          ctypes.c_uint32, ctypes.c_void_p]
     lib.attn_score_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_score_workspace_bytes.argtypes = [PT, PT, PT, ctypes.c_int32]
+    lib.attn_sparse_bwd.restype = ctypes.c_int
+    lib.attn_sparse_bwd.argtypes = [PT, PT, PT, PT, PT, PT, PT, PT, ctypes.c_float, PT, PT, PT,
+                                    ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint32,
+                                    ctypes.c_void_p]
+    lib.attn_sparse_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_sparse_bwd_workspace_bytes.argtypes = [PT, PT, ctypes.c_int]
     lib.attn_bwd.restype = ctypes.c_int
     lib.attn_bwd.argtypes = [PT, PT, PT, PT, PT, PT, PT, PT, ctypes.c_int32, ctypes.c_int,
                              ctypes.c_float, PT, PT, PT, ctypes.c_void_p, ctypes.c_size_t,

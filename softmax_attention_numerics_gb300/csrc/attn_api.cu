@@ -598,6 +598,164 @@ extern "C" int attn_score_recompute(const attn_tensor_t* q, const attn_tensor_t*
     return run_stage(ATTN_STAGE_SCORE, st, [&] { return launch_score_recompute(p, st); });
 }
 
+namespace attn {
+namespace {
+
+// Sparse top-k backward: the shape contract, every tensor against q
+// (NVIDIA/cudnn-frontend PR #429: a transposed dout or lse, a mis-shaped
+// index tensor or an unsupported head dim must fail before launch).
+struct SparseShapes {
+    int elt;
+    int64_t B, S, H, D, Skv, K;
+};
+
+int sparse_shapes(const attn_tensor_t* q, const attn_tensor_t* kv, SparseShapes* s) {
+    if (!q || !kv) return ATTN_E_ARG;
+    if (q->dtype != ATTN_BF16 && q->dtype != ATTN_F16) return ATTN_E_DTYPE;
+    s->elt = q->dtype;
+    ATTN_TRY(check_input(q, 4, s->elt));
+    s->B = q->shape[0];
+    s->S = q->shape[1];
+    s->H = q->shape[2];
+    s->D = q->shape[3];
+    if (s->H != 64 || (s->D != 512 && s->D != 576)) return ATTN_E_UNSUPPORTED;
+    ATTN_TRY(check_input(kv, 3, s->elt));
+    if (kv->shape[0] != s->B || kv->shape[2] != s->D) return ATTN_E_SHAPE;
+    s->Skv = kv->shape[1];
+    if (s->B * s->S > INT32_MAX / 2 || s->Skv > INT32_MAX / 2) return ATTN_E_SHAPE;
+    return ATTN_OK;
+}
+
+struct SparseWs {
+    size_t acc, delta, sink, total;
+};
+
+SparseWs sparse_ws(const SparseShapes& s, bool with_sink) {
+    SparseWs w;
+    const size_t vec = round256(static_cast<size_t>(s.B * s.S * s.H) * 4);
+    w.acc = 0;
+    w.delta = round256(static_cast<size_t>(s.B * s.Skv * s.D) * 4);
+    w.sink = w.delta + vec;
+    w.total = w.sink + (with_sink ? vec : 0);
+    return w;
+}
+
+// int32 index tensor: the given shape, contiguous, 4-byte aligned.
+int check_index(const attn_tensor_t* t, const int64_t* shape, int rank) {
+    if (!t) return ATTN_E_ARG;
+    if (t->dtype != ATTN_I32) return ATTN_E_DTYPE;
+    if (!same_shape(t, shape, rank)) return ATTN_E_SHAPE;
+    int64_t n = 1;
+    for (int i = 0; i < rank; ++i) n *= shape[i];
+    if (n > 0 && !t->data) return ATTN_E_ARG;
+    if (!is_contiguous(t)) return ATTN_E_LAYOUT;
+    if ((reinterpret_cast<uintptr_t>(t->data) & 3u) != 0) return ATTN_E_LAYOUT;
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" size_t attn_sparse_bwd_workspace_bytes(const attn_tensor_t* q, const attn_tensor_t* kv,
+                                                  int with_sink) {
+    attn::SparseShapes s;
+    if (attn::sparse_shapes(q, kv, &s) != ATTN_OK) return 0;
+    return attn::sparse_ws(s, with_sink != 0).total;
+}
+
+extern "C" int attn_sparse_bwd(const attn_tensor_t* q, const attn_tensor_t* kv,
+                               const attn_tensor_t* out, const attn_tensor_t* dout,
+                               const attn_tensor_t* lse, const attn_tensor_t* attn_sink,
+                               const attn_tensor_t* topk_idxs, const attn_tensor_t* topk_length,
+                               float scale, attn_tensor_t* dq, attn_tensor_t* dkv,
+                               attn_tensor_t* d_sink, void* workspace, size_t workspace_bytes,
+                               uint32_t flags, attn_stream_t stream) {
+    using namespace attn;
+    if (flags != 0) return ATTN_E_ARG;
+    if (!isfinite(scale)) return ATTN_E_ARG;
+    SparseShapes s;
+    ATTN_TRY(sparse_shapes(q, kv, &s));
+    const int64_t oshape[4] = {s.B, s.S, s.H, 512};
+    ATTN_TRY(check_input(out, 4, s.elt));
+    ATTN_TRY(check_input(dout, 4, s.elt));
+    if (!same_shape(out, oshape, 4) || !same_shape(dout, oshape, 4)) return ATTN_E_SHAPE;
+    const int64_t lshape[3] = {s.B, s.S, s.H};
+    ATTN_TRY(check_output(lse, ATTN_F32, lshape, 3));
+    if (!topk_idxs) return ATTN_E_ARG;
+    if (topk_idxs->ndim != 3) return ATTN_E_SHAPE;
+    s.K = topk_idxs->shape[2];
+    const int64_t ishape[3] = {s.B, s.S, s.K};
+    ATTN_TRY(check_index(topk_idxs, ishape, 3));
+    const int64_t nshape[2] = {s.B, s.S};
+    if (topk_length) ATTN_TRY(check_index(topk_length, nshape, 2));
+    const int64_t hshape[1] = {s.H};
+    if ((attn_sink == nullptr) != (d_sink == nullptr)) return ATTN_E_ARG;
+    if (attn_sink) {
+        ATTN_TRY(check_output(attn_sink, ATTN_F32, hshape, 1));
+        ATTN_TRY(check_output(d_sink, ATTN_F32, hshape, 1));
+    }
+    ATTN_TRY(check_output(dq, s.elt, q->shape, 4));
+    ATTN_TRY(check_output(dkv, s.elt, kv->shape, 3));
+    const SparseWs w = sparse_ws(s, attn_sink != nullptr);
+    if (!workspace || workspace_bytes < w.total) return ATTN_E_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_E_WORKSPACE;
+    int dev;
+    ATTN_TRY(current_device(&dev));
+    for (const attn_tensor_t* t : {q, kv, out, dout, lse, attn_sink, topk_idxs, topk_length,
+                                   static_cast<const attn_tensor_t*>(dq),
+                                   static_cast<const attn_tensor_t*>(dkv),
+                                   static_cast<const attn_tensor_t*>(d_sink)})
+        ATTN_TRY(check_device(t, dev));
+    SparseProblem p{};
+    p.err = error_word(dev);
+    if (!p.err) return ATTN_E_CUDA;
+    p.q = static_cast<const bf16*>(q->data);
+    p.kv = static_cast<const bf16*>(kv->data);
+    p.out = static_cast<const bf16*>(out->data);
+    p.dout = static_cast<const bf16*>(dout->data);
+    p.lse = static_cast<const float*>(lse->data);
+    p.sink = attn_sink ? static_cast<const float*>(attn_sink->data) : nullptr;
+    p.idx = static_cast<const int*>(topk_idxs->data);
+    p.len = topk_length ? static_cast<const int*>(topk_length->data) : nullptr;
+    p.dq = static_cast<bf16*>(dq->data);
+    p.dkv = static_cast<bf16*>(dkv->data);
+    p.dsink = d_sink ? static_cast<float*>(d_sink->data) : nullptr;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.dkv_acc = reinterpret_cast<float*>(ws + w.acc);
+    p.delta = reinterpret_cast<float*>(ws + w.delta);
+    p.dsink_part = attn_sink ? reinterpret_cast<float*>(ws + w.sink) : nullptr;
+    p.q_b = q->stride[0], p.q_s = q->stride[1], p.q_h = q->stride[2];
+    p.kv_b = kv->stride[0], p.kv_s = kv->stride[1];
+    p.o_b = out->stride[0], p.o_s = out->stride[1], p.o_h = out->stride[2];
+    p.do_b = dout->stride[0], p.do_s = dout->stride[1], p.do_h = dout->stride[2];
+    p.idx_b = s.S * s.K, p.idx_s = s.K;
+    p.len_b = s.S, p.len_s = 1;
+    p.B = static_cast<int>(s.B), p.S = static_cast<int>(s.S), p.Skv = static_cast<int>(s.Skv);
+    p.H = static_cast<int>(s.H), p.Dqk = static_cast<int>(s.D), p.Dv = 512;
+    p.K = static_cast<int>(s.K);
+    p.f16 = s.elt == ATTN_F16;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.debug_stall = debug_stall_point();
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    const size_t acc_bytes = static_cast<size_t>(s.B * s.Skv * s.D) * 4;
+    if (acc_bytes > 0 && (e = cudaMemsetAsync(p.dkv_acc, 0, acc_bytes, st)) != cudaSuccess)
+        return cuda_fail(e, "dkv workspace zero-fill");
+    ATTN_TRY(run_stage(-1, st, [&] { return launch_sparse_prep(p, st); }));
+    if (s.Skv > 0) {
+        ATTN_TRY(run_stage(ATTN_STAGE_SPARSE, st, [&] { return launch_sparse_bwd_main(p, st); }));
+    } else {
+        // no kv row exists, so no entry takes part: dq is zero
+        const size_t dq_bytes = static_cast<size_t>(s.B * s.S * s.H * s.D) * 2;
+        if (dq_bytes > 0 && (e = cudaMemsetAsync(p.dq, 0, dq_bytes, st)) != cudaSuccess)
+            return cuda_fail(e, "dq zero-fill");
+    }
+    ATTN_TRY(run_stage(-1, st, [&] { return launch_sparse_dkv_convert(p, st); }));
+    if (attn_sink) ATTN_TRY(run_stage(-1, st, [&] { return launch_sparse_dsink(p, st); }));
+    return ATTN_OK;
+}
+
 extern "C" int attn_get_error(attn_stream_t stream) {
     int dev;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_E_CUDA;
@@ -669,7 +827,7 @@ extern "C" int attn_debug_inject_stall(int kernel, int iteration) {
         g_debug_stall.store(-1);
         return ATTN_OK;
     }
-    if (kernel > 5 || iteration < 0 || iteration > 0xffff) return ATTN_E_ARG;
+    if (kernel > 6 || iteration < 0 || iteration > 0xffff) return ATTN_E_ARG;
     g_debug_stall.store((kernel << 16) | iteration);
     return ATTN_OK;
 }

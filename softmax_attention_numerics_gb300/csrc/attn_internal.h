@@ -87,6 +87,11 @@ int debug_stall_point();
 bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t S, int64_t B,
                    int64_t sh, int64_t ss, int64_t sb, bool f16);
 
+// TMA tensor map over a 16-bit [B, S, H, D] view with box 64 x 64 x 1 x 1
+// (64 columns of 64 heads of one token), 128-byte swizzle; H >= 64.
+bool make_heads_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t S, int64_t B,
+                    int64_t sh, int64_t ss, int64_t sb, bool f16);
+
 // TMA tensor map over the fp32 dQ workspace [R, H, D] (dims D, H, R), box
 // 32 x 1 x 128, 128-byte swizzle; the target of bulk reduce-adds.
 bool make_f32_reduce_map(CUtensorMap* m, void* base, int64_t D, int64_t H, int64_t R);
@@ -121,6 +126,40 @@ struct Fp8Problem {
 bool make_u8_map(CUtensorMap* m, const void* base, const int64_t dims[4], const int64_t strides[3],
                  int box1, int box2);
 
+// Sparse top-k (DSA) backward: q [B,S,H,Dqk], kv [B,Skv,Dqk] (one row set
+// shared by the H query heads; values are its first Dv = 512 columns), out /
+// dout [B,S,H,Dv], lse [B,S,H] fp32 (natural log, the sink included),
+// topk_idxs int32 [B,S,K], optional topk_length int32 [B,S], optional sink
+// fp32 [H].  H = 64, Dqk = 512 or 576.  Strides in elements.
+struct SparseProblem {
+    const bf16* q;
+    const bf16* kv;
+    const bf16* out;
+    const bf16* dout;
+    const float* lse;        // contiguous [B, S, H]
+    const float* sink;       // [H] or null
+    const int* idx;
+    const int* len;          // [B, S] or null
+    bf16* dq;                // contiguous like q
+    bf16* dkv;               // contiguous like kv
+    float* dsink;            // [H] (when sink)
+    float* dkv_acc;          // workspace: fp32 [B * Skv, Dqk]
+    float* delta;            // workspace: fp32 [B * S, H]
+    float* dsink_part;       // workspace: fp32 [B * S, H] (when sink)
+    int64_t q_b, q_s, q_h;
+    int64_t kv_b, kv_s;
+    int64_t o_b, o_s, o_h;
+    int64_t do_b, do_s, do_h;
+    int64_t idx_b, idx_s;    // topk_idxs: b * idx_b + i * idx_s + e
+    int64_t len_b, len_s;    // topk_length: b * len_b + i * len_s
+    int B, S, Skv, H, Dqk, Dv, K;
+    int f16;
+    float scale;
+    float scale_log2;        // scale * log2(e)
+    int* err;
+    int debug_stall;
+};
+
 // Launchers (each enqueues on `stream`, returns cudaGetLastError()).
 cudaError_t launch_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const Problem& p, cudaStream_t stream);
@@ -129,6 +168,12 @@ cudaError_t launch_bwd_dq_convert(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_deterministic(const Problem& p, cudaStream_t stream);
 cudaError_t launch_zero_trailing_fwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_score_recompute(const Problem& p, cudaStream_t stream);
+// Sparse backward stages: Delta (and the sink terms), the main kernel, the
+// dkv conversion, the ordered d_sink sum.
+cudaError_t launch_sparse_prep(const SparseProblem& p, cudaStream_t stream);
+cudaError_t launch_sparse_bwd_main(const SparseProblem& p, cudaStream_t stream);
+cudaError_t launch_sparse_dkv_convert(const SparseProblem& p, cudaStream_t stream);
+cudaError_t launch_sparse_dsink(const SparseProblem& p, cudaStream_t stream);
 int score_key_tiles(int64_t width);
 cudaError_t launch_zero_trailing_bwd(const Problem& p, cudaStream_t stream);
 cudaError_t launch_fp8_transpose_v(const Fp8Problem& p, cudaStream_t stream);

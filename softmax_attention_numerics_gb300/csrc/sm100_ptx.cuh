@@ -115,7 +115,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 // completes at that point, so that the kernel's own unwind paths run:
 // the abort flag, the drains of copies and MMAs in flight, ATTN_E_TIMEOUT.
 constexpr uint64_t kDebugStallBudgetNs = 200000ull;     // 200 us
-enum { kStallFwd = 1, kStallBwd = 2, kStallDq = 3, kStallFp8 = 4, kStallScore = 5 };
+enum { kStallFwd = 1, kStallBwd = 2, kStallDq = 3, kStallFp8 = 4, kStallScore = 5, kStallSparse = 6 };
 
 __device__ __forceinline__ bool dbg_check(bool ok, int* err) {
 #ifdef ATTN_DEBUG_CHECKS

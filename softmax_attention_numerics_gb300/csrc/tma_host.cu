@@ -45,6 +45,24 @@ bool make_tile_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64
            CUDA_SUCCESS;
 }
 
+bool make_heads_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t S, int64_t B,
+                    int64_t sh, int64_t ss, int64_t sb, bool f16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(S > 0 ? S : 1),
+                          (cuuint64_t)(B > 0 ? B : 1)};
+    cuuint64_t strides[3] = {(cuuint64_t)(sh * 2), (cuuint64_t)(ss * 2), (cuuint64_t)(sb * 2)};
+    // Strides of size-1 dims are never used; keep them legal (16-byte multiples).
+    if (dims[2] == 1) strides[1] = strides[0] * dims[1];
+    if (dims[3] == 1) strides[2] = strides[1] * dims[2];
+    cuuint32_t box[4] = {64, 64, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_f32_reduce_map(CUtensorMap* m, void* base, int64_t D, int64_t H, int64_t R) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;

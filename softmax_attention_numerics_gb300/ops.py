@@ -169,6 +169,44 @@ def attn_score_recompute(q, k, lse, cu_seqlens=None, max_seqlen=None, causal=Fal
     return score, l1
 
 
+def sparse_bwd_workspace_bytes(q, kv, with_sink):
+    lib = _lib.load()
+    q_, kv_ = tensor_desc(q), tensor_desc(kv)
+    return int(lib.attn_sparse_bwd_workspace_bytes(ctypes.byref(q_), ctypes.byref(kv_),
+                                                   1 if with_sink else 0))
+
+
+def attn_sparse_bwd(q, kv, out, dout, lse, topk_idxs, topk_length=None, attn_sink=None,
+                    scale=None, dq=None, dkv=None, d_sink=None, workspace=None, stream=None):
+    """Backward of sparse top-k attention with an attention sink.
+
+    q [B,S,64,Dqk] (Dqk 512 or 576), kv [B,S_kv,Dqk], out / dout [B,S,64,512],
+    lse [B,S,64] fp32, topk_idxs int32 [B,S,K], topk_length int32 [B,S] or
+    None, attn_sink fp32 [64] or None.  Returns (dq, dkv, d_sink); d_sink is
+    None without a sink.  scale=None means 1/sqrt(Dqk).
+    """
+    lib = _lib.load()
+    s = _stream(stream, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    with torch.cuda.device(q.device), torch.cuda.stream(s):
+        dq = torch.empty(q.shape, dtype=q.dtype, device=q.device) if dq is None else dq
+        dkv = torch.empty(kv.shape, dtype=kv.dtype, device=kv.device) if dkv is None else dkv
+        if attn_sink is not None and d_sink is None:
+            d_sink = torch.empty(attn_sink.shape, dtype=torch.float32, device=q.device)
+        nbytes = sparse_bwd_workspace_bytes(q, kv, attn_sink is not None)
+        if workspace is None or workspace.numel() < nbytes:
+            workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+        descs = [tensor_desc(x) for x in (q, kv, out, dout, lse, attn_sink, topk_idxs,
+                                          topk_length, dq, dkv, d_sink)]
+        rc = lib.attn_sparse_bwd(*[_ref(d) for d in descs[:8]], float(scale),
+                                 *[_ref(d) for d in descs[8:]],
+                                 ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), 0,
+                                 ctypes.c_void_p(s.cuda_stream))
+    _lib.check(rc, "attn_sparse_bwd")
+    return dq, dkv, d_sink
+
+
 def bwd_workspace_bytes(q, k, deterministic=False):
     lib = _lib.load()
     dq_, dk_ = tensor_desc(q), tensor_desc(k)

@@ -395,7 +395,7 @@ def test_checked_variant_builds_and_exports_the_abi_and_the_stall_hook():
     fn = dbg.attn_debug_inject_stall
     fn.restype = ctypes.c_int
     fn.argtypes = [ctypes.c_int, ctypes.c_int]
-    assert fn(6, 0) == E["ATTN_E_ARG"]
+    assert fn(7, 0) == E["ATTN_E_ARG"]
     assert fn(1, -1) == E["ATTN_E_ARG"]
     assert fn(2, 70000) == E["ATTN_E_ARG"]
     assert fn(2, 3) == 0
@@ -419,3 +419,65 @@ def test_use_library_swaps_and_restores(lib):
         with _lib.use_library(os.path.join(build.LIB_DIR, "missing.so")):
             pass
     assert _lib.load() is before
+
+
+def sparse(B=2, S=100, Skv=300, H=64, D=576, K=128, sink=True, length=True):
+    return dict(q=desc([B, S, H, D]), kv=desc([B, Skv, D]), out=desc([B, S, H, 512]),
+                dout=desc([B, S, H, 512]), lse=desc([B, S, H], _lib.ATTN_F32),
+                sink=desc([H], _lib.ATTN_F32) if sink else None,
+                idx=desc([B, S, K], _lib.ATTN_I32),
+                len=desc([B, S], _lib.ATTN_I32) if length else None,
+                dq=desc([B, S, H, D]), dkv=desc([B, Skv, D]),
+                dsink=desc([H], _lib.ATTN_F32) if sink else None)
+
+
+def call_sparse(lib, t, scale=0.04, ws=FAKE, ws_bytes=1 << 40, flags=0):
+    return lib.attn_sparse_bwd(R(t["q"]), R(t["kv"]), R(t["out"]), R(t["dout"]), R(t["lse"]),
+                               R(t["sink"]), R(t["idx"]), R(t["len"]), scale, R(t["dq"]),
+                               R(t["dkv"]), R(t["dsink"]), ctypes.c_void_p(ws), ws_bytes, flags,
+                               None)
+
+
+def test_sparse_bwd_contract(lib):
+    """NVIDIA/cudnn-frontend PR #429: every companion tensor of the DSA
+    backward is checked against q before launch (a transposed dout or lse, a
+    mis-shaped index tensor, a wrong dtype, a strided out-parameter or an
+    unsupported head dim fails instead of running)."""
+    stop = (E["ATTN_E_DEVICE"], E["ATTN_E_CUDA"])
+    assert call_sparse(lib, sparse()) in stop                          # valid: stops at the device
+    assert call_sparse(lib, sparse(D=512, sink=False, length=False)) in stop
+    assert call_sparse(lib, sparse(K=0)) in stop
+    assert call_sparse(lib, sparse(), flags=1) == E["ATTN_E_ARG"]
+    assert call_sparse(lib, sparse(), scale=float("nan")) == E["ATTN_E_ARG"]
+    assert call_sparse(lib, sparse(H=32)) == E["ATTN_E_UNSUPPORTED"]
+    assert call_sparse(lib, sparse(D=128)) == E["ATTN_E_UNSUPPORTED"]
+
+    def bad(key, value, code):
+        t = sparse()
+        t[key] = value
+        assert call_sparse(lib, t) == E[code], (key, code)
+
+    bad("dout", desc([2, 100, 512, 64]), "ATTN_E_SHAPE")               # transposed dout
+    bad("lse", desc([2, 64, 100], _lib.ATTN_F32), "ATTN_E_SHAPE")      # transposed lse
+    bad("lse", desc([2, 100, 64]), "ATTN_E_DTYPE")                     # bf16 lse
+    bad("kv", desc([2, 300, 512]), "ATTN_E_SHAPE")
+    bad("kv", desc([1, 300, 576]), "ATTN_E_SHAPE")
+    bad("out", desc([2, 100, 64, 512], _lib.ATTN_F16), "ATTN_E_DTYPE")
+    bad("idx", desc([2, 99, 128], _lib.ATTN_I32), "ATTN_E_SHAPE")
+    bad("idx", desc([2, 100, 128], _lib.ATTN_F32), "ATTN_E_DTYPE")
+    bad("idx", desc([2, 100, 128], _lib.ATTN_I32, stride=[100 * 256, 256, 1]), "ATTN_E_LAYOUT")
+    bad("len", desc([2, 101], _lib.ATTN_I32), "ATTN_E_SHAPE")
+    bad("sink", desc([32], _lib.ATTN_F32), "ATTN_E_SHAPE")
+    bad("sink", None, "ATTN_E_ARG")                                    # d_sink without a sink
+    bad("dsink", None, "ATTN_E_ARG")                                   # a sink without d_sink
+    bad("dq", desc([2, 100, 64, 576], stride=[100 * 64 * 640, 64 * 640, 640, 1]), "ATTN_E_LAYOUT")
+    bad("dkv", desc([2, 300, 576], _lib.ATTN_F16), "ATTN_E_DTYPE")
+    bad("q", desc([2, 100, 64, 576], _lib.ATTN_F32), "ATTN_E_DTYPE")
+    bad("idx", None, "ATTN_E_ARG")
+    t = sparse()
+    n = lib.attn_sparse_bwd_workspace_bytes(R(t["q"]), R(t["kv"]), 1)
+    vec = -(-2 * 100 * 64 * 4 // 256) * 256
+    assert n == -(-2 * 300 * 576 * 4 // 256) * 256 + 2 * vec
+    assert lib.attn_sparse_bwd_workspace_bytes(R(t["q"]), R(t["kv"]), 0) == n - vec
+    assert call_sparse(lib, t, ws_bytes=n - 1) == E["ATTN_E_WORKSPACE"]
+    assert call_sparse(lib, t, ws=FAKE + 16, ws_bytes=n) == E["ATTN_E_WORKSPACE"]
