@@ -50,8 +50,14 @@ def parse(argv=None):
                          "forward alone (bf16 out)")
     ap.add_argument("--deterministic", action="store_true",
                     help="dQ by the per-query-tile kernel instead of fp32 reductions")
-    ap.add_argument("--workload", default="attention", choices=["attention", "score"],
-                    help="score: the head-summed score recompute (its own metric and line)")
+    ap.add_argument("--workload", default="attention", choices=["attention", "score", "sparse"],
+                    help="score: the head-summed score recompute; sparse: the sparse top-k "
+                         "backward with a sink (each its own metric and line)")
+    ap.add_argument("--sparse-dim", type=int, default=576, choices=[512, 576],
+                    help="kv row width of the sparse workload (576: values in the first 512)")
+    ap.add_argument("--topk", type=int, default=128, help="index entries per token (sparse)")
+    ap.add_argument("--sparse-batch", type=int, default=16,
+                    help="sequences of 512 queries over 2048 kv rows (sparse)")
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="kv heads of the score workload (0: 1, all q heads share it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -520,6 +526,170 @@ def run_score(a):
     print(json.dumps(line))
 
 
+def sparse_inputs(B, S, Skv, H, D, K, seed, dev):
+    """Seeded sparse-workload inputs drawn on the device (the same recipe as
+    attn_workloads.dsa_case: N(0,1) q, kv, dout; K distinct uniform rows per
+    token; N(0,1) sink), plus the forward's out and lse from plain torch
+    products in fp32 (input preparation, not timed)."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(seed)
+    q = torch.randn(B, S, H, D, generator=g, device=dev).to(torch.bfloat16)
+    kv = torch.randn(B, Skv, D, generator=g, device=dev).to(torch.bfloat16)
+    dout = torch.randn(B, S, H, 512, generator=g, device=dev).to(torch.bfloat16)
+    idx = torch.rand(B, S, Skv, generator=g, device=dev).argsort(dim=2)[:, :, :K]
+    idx = idx.to(torch.int32).contiguous()
+    sink = torch.randn(H, generator=g, device=dev)
+    scale = 1.0 / math.sqrt(D)
+    out = torch.empty(B, S, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, S, H, dtype=torch.float32, device=dev)
+    for b in range(B):
+        ksel = kv[b].float()[idx[b].long()]                                # [S, K, D]
+        s_ = torch.einsum("shd,skd->shk", q[b].float(), ksel) * scale
+        logits = torch.cat([s_, sink.view(1, H, 1).expand(S, H, 1)], dim=2)
+        lse[b] = torch.logsumexp(logits, dim=2)
+        w = torch.exp(s_ - lse[b][..., None])
+        out[b] = torch.einsum("shk,skd->shd", w, ksel[..., :512]).to(torch.bfloat16)
+    return dict(q=q, kv=kv, out=out, dout=dout, lse=lse, idx=idx, sink=sink, scale=scale)
+
+
+def sparse_cpu_baseline(D, K, tokens=2048, seed=42):
+    """The fp64 oracle on `tokens` tokens of the same shapes (S_kv = 2048,
+    H = 64, full index lists, a sink), in this process before any GPU work."""
+    import numpy as np
+    from oracle import sparse_oracle as OS
+    rng = np.random.default_rng(seed)
+    S, Skv, H = tokens, 2048, 64
+    q = rng.standard_normal((1, S, H, D)).astype(np.float32).astype(np.float64)
+    kv = rng.standard_normal((1, Skv, D)).astype(np.float32).astype(np.float64)
+    do = rng.standard_normal((1, S, H, 512)).astype(np.float32).astype(np.float64)
+    idx = np.stack([rng.permutation(Skv)[:K] for _ in range(S)])[None].astype(np.int32)
+    sink = rng.standard_normal(H)
+    t0 = time.perf_counter()
+    OS.dsa_bwd(q, kv, do, idx, None, sink, scale=1.0 / math.sqrt(D), dv=512)
+    dt = time.perf_counter() - t0
+    flops = S * K * H * (6.0 * D + 4.0 * 512)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count() or 1,
+            "kind": "oracle",
+            "sample": "fp64 numpy oracle (forward + backward) of %d tokens x %d entries x %d heads, "
+                      "D=%d, S_kv=2048, with a sink (%.3g flop in %.2f s)" % (S, K, H, D, flops, dt)}
+
+
+def run_sparse(a):
+    """--workload sparse: the sparse top-k (DSA) backward with an attention
+    sink at the shape of NVIDIA/cudnn-frontend PR #429's check (S = 512
+    queries over S_kv = 2048 kv rows, H = 64, D = 576 / values 512, top-k =
+    128), `--sparse-batch` sequences per step.  One step = attn_sparse_bwd on
+    resident inputs (zero-fill, Delta, main kernel, dkv conversion, d_sink).
+    Work: (6 D + 4 * 512) flop per (token, entry, head) on the tensor cores."""
+    import torch
+    cpu = None if a.no_cpu_baseline else sparse_cpu_baseline(a.sparse_dim, a.topk)
+    from softmax_attention_numerics_gb300 import _lib, attn_sparse_bwd, sparse_bwd_workspace_bytes
+    from softmax_attention_numerics_gb300 import build as _build
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    lib = _lib.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B, S, Skv, H, D, K = a.sparse_batch, 512, 2048, 64, a.sparse_dim, a.topk
+    x = sparse_inputs(B, S, Skv, H, D, K, 42, dev)
+    dq = torch.empty_like(x["q"])
+    dkv = torch.empty_like(x["kv"])
+    ds = torch.empty(H, dtype=torch.float32, device=dev)
+    ws = torch.empty(sparse_bwd_workspace_bytes(x["q"], x["kv"], True), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        attn_sparse_bwd(x["q"], x["kv"], x["out"], x["dout"], x["lse"], x["idx"],
+                        attn_sink=x["sink"], scale=x["scale"], dq=dq, dkv=dkv, d_sink=ds,
+                        workspace=ws, stream=stream)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(a.steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in ev:
+            e0.record(stream)
+            e1.record(stream)
+        for _ in range(a.warmup):
+            step()
+    stream.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = lib.attn_launch_count()
+    with ClockSampler(0) as clk:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(a.steps):
+                lib.attn_profile_events(_lib.ATTN_STAGE_SPARSE, ctypes_ptr(ev[i][0]),
+                                        ctypes_ptr(ev[i][1]))
+                step()
+            t1.record(stream)
+        lib.attn_profile_events(_lib.ATTN_STAGE_SPARSE, None, None)
+        stream.synchronize()
+    launches = lib.attn_launch_count() - launches0
+    ms = t0.elapsed_time(t1) / a.steps
+    kern_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    tokens = B * S
+    flops = tokens * K * H * (6.0 * D + 4.0 * 512)
+    # algorithmic bytes of the main kernel: q, dout read and dq written once,
+    # the kv rows read once, the fp32 dkv accumulator read and written once,
+    # the index lists, lse and Delta
+    nbytes = (tokens * H * (2 * D * 2 + 512 * 2) + B * Skv * D * (2 + 8) + tokens * K * 4
+              + tokens * H * 8)
+    peaks, kind = measured_peaks()
+    burst, bw = peaks.get("bf16_tflops", 1900.0), peaks.get("hbm_gbs", 6800.0)
+    tf = flops / (kern_ms / 1e3) / 1e12
+    gbs = nbytes / (kern_ms / 1e3) / 1e9
+    t_flop, t_byte = flops / (burst * 1e12), nbytes / (bw * 1e9)
+    if t_byte > t_flop:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": bw, "unit": "GB/s", "frac": gbs / bw}
+    else:
+        roof = {"bound": "tensor", "achieved": tf, "peak": burst, "unit": "TFLOP/s", "frac": tf / burst}
+    roof.update({"kernel": "sparse_bwd_sm100", "traffic": None, "peak_source": kind,
+                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                 "tensor_tflops": tf, "tensor_frac": tf / burst, "hbm_gbs": gbs, "hbm_frac": gbs / bw})
+    nonfinite = sum(int((~torch.isfinite(t.float())).sum()) for t in (dq, dkv, ds))
+    # e2e: every input from pinned host memory, dq / dkv / d_sink back, each step
+    names = ("q", "kv", "out", "dout", "lse", "idx", "sink")
+    host_in = [x[n].cpu().pin_memory() for n in names]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dkv, ds)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e_steps = max(1, min(a.steps, 3))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e_steps):
+            for n, src in zip(names, host_in):
+                x[n].copy_(src, non_blocking=True)
+            step()
+            for dst, src in zip(host_out, (dq, dkv, ds)):
+                dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    line = {
+        "metric": "sparse top-k attention backward TFLOP/s (dq, dkv, d_sink)",
+        "value": flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "dsa_bwd B=%d S=512 S_kv=2048 H=64 D=%d/512 top-k=%d sink" % (B, D, K),
+                   "B": B, "S": S, "S_kv": Skv, "H": H, "D": D, "Dv": 512, "topk": K,
+                   "sink": True, "topk_length": False, "parallelism": "single",
+                   "l2": "no flush: q, dout and dq (%d MiB) exceed L2" % (
+                       tokens * H * (2 * D + 512) * 2 / 2 ** 20)},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "extra": {"kernel_ms": kern_ms, "nonfinite_outputs": nonfinite,
+                  "tokens_per_s": tokens / (ms / 1e3)},
+    }
+    print(json.dumps(line))
+
+
 # ---------------------------------------------------------------- our arm
 
 def main():
@@ -534,6 +704,11 @@ def main():
         if int(os.environ.get("WORLD_SIZE", "1")) > 1:
             raise SystemExit("--workload score: one GPU")
         run_score(a)
+        return
+    if a.workload == "sparse":
+        if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+            raise SystemExit("--workload sparse: one GPU")
+        run_sparse(a)
         return
     if a.dtype == "e4m3":
         if a.head_dim != 128 or a.deterministic or int(os.environ.get("WORLD_SIZE", "1")) > 1:

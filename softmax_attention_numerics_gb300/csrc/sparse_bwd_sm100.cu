@@ -23,12 +23,19 @@
 //   dKV  [128 e x 64 d]  = dS^T . Q[:, d] + P^T . dO[:, d]   (A from TMEM)
 // Roles (256 threads, so that no register cap below 255 applies):
 //   warps 0-3  one entry per thread (TMEM lane): P^T, dS^T; the dKV rows,
-//              bulk-reduced (fp32 add) into the workspace row idx_e; dq
-//   warps 4-5  gather the 128 selected kv rows (two per thread) with 16-byte
-//              cp.async into the 128-byte-swizzled operand layout (the rows
-//              stay resident for S^T, dP^T and dQ^T)
-//   warp 6     TMA: 64 x 64 blocks of Q and dO through a 3-stage ring, in
-//              the order the MMA issuer consumes them (twice per item)
+//              bulk-reduced (fp32 add) into the workspace row idx_e in two
+//              half-row operations, staged in the gathered-rows region once
+//              dQ^T no longer reads it (a few large bulk operations instead
+//              of many small ones: their count, not their bytes, is the
+//              limit); dq
+//   warps 4-5  gather the 128 selected kv rows with 16-byte cp.async (each
+//              warp instruction covers whole 128-byte row blocks) into the
+//              128-byte-swizzled operand layout (the rows stay resident for
+//              S^T, dP^T and dQ^T)
+//   warp 6     TMA: the 64 x 64 blocks of Q and dO of one 64-column slice
+//              together through a 3-stage ring (one wait and one release per
+//              slice), in the order the MMA issuer consumes them (twice per
+//              item); an L2 prefetch of the next token's blocks
 //   warp 7     TMEM allocator and single-thread UMMA issuer
 // TMEM: S^T at 0 (P^T packed over its first 32 columns, dS^T over the next
 // 32), dP^T at 64 (after use: dKV buffer 1), dQ^T at 128 + 64 m, dKV buffer 0
@@ -45,22 +52,22 @@ constexpr int kSpH = 64;             // query heads per token
 constexpr int kSpE = 128;            // index entries per work item
 constexpr int kSpDv = 512;           // value columns
 constexpr int kSpThreads = 256;
-constexpr int kRing = 3;             // Q / dO block ring (8 KB stages)
-constexpr int kStageRow = 144;       // staging row: 128 data bytes + 16 of padding (bank spread)
-constexpr int kStageSlot = 32 * kStageRow;
+constexpr int kRing = 3;             // ring of (Q block, dO block) pairs, 16 KB a stage
 
 template <int NB>   // 64-column blocks of the kv rows: 8 (512) or 9 (576)
 struct SpLayout {
     static constexpr int kNBV = kSpDv / 64;
     static constexpr int kNM = (NB + 1) / 2;                // dQ^T chunks of 128 columns
     static constexpr int kKV = 0;                           // NB x [128 entries][64 cols] bf16
-    static constexpr int kRingOff = NB * 16384;             // kRing x [64 heads][64 cols] bf16
-    static constexpr int kDS = kRingOff + kRing * 8192;     // dS^T [128 entries][64 heads] bf16
-    static constexpr int kStage = kDS + 16384;              // 4 warps x 2 slots x 32 rows
-    static constexpr int kBar = kStage + 8 * kStageSlot;
-    static constexpr int kBarKV = 0;                        // NB: gathered block landed (64)
-    static constexpr int kBarRFull = NB, kBarREmpty = NB + kRing;
-    static constexpr int kBarSdp = NB + 2 * kRing;          // S^T and dP^T complete
+    // dKV staging over the same region during the dKV phase: 128 rows of half
+    // a kv row in fp32 (NB x 128 bytes) + 16 bytes of padding (bank spread)
+    static constexpr int kStRow = NB * 128 + 16;
+    static constexpr int kRingOff = 128 * kStRow;           // kRing x {Q, dO} x [64 heads][64 cols] bf16
+    static constexpr int kDS = kRingOff + kRing * 16384;    // dS^T [128 entries][64 heads] bf16
+    static constexpr int kBar = kDS + 16384;
+    static constexpr int kBarKV = 0;                        // gathered rows landed (64)
+    static constexpr int kBarRFull = 1, kBarREmpty = 1 + kRing;
+    static constexpr int kBarSdp = 1 + 2 * kRing;           // S^T and dP^T complete
     static constexpr int kBarPds = kBarSdp + 1;             // P^T, dS^T written (128)
     static constexpr int kBarKVFree = kBarPds + 1;          // gathered rows no longer read
     static constexpr int kBarDkvFull = kBarKVFree + 1;      // 2
@@ -68,7 +75,8 @@ struct SpLayout {
     static constexpr int kBarItemDone = kBarDkvFree + 2;    // every dKV chunk read out (128)
     static constexpr int kBarDQFull = kBarItemDone + 1;
     static constexpr int kBarDQRead = kBarDQFull + 1;       // dQ^T read out (128)
-    static constexpr int kBarDrain = kBarDQRead + 1;
+    static constexpr int kBarStageFree = kBarDQRead + 1;    // staging read by the bulk adds (128)
+    static constexpr int kBarDrain = kBarStageFree + 1;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16 + 1024;        // + alignment slack
@@ -76,6 +84,7 @@ struct SpLayout {
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kColDQ + 64 * kNM <= kColKV0, "TMEM columns");
     static_assert(kBytes <= 232448, "shared memory");
+    static_assert(kRingOff % 1024 == 0 && kRingOff >= NB * 16384, "ring placement");
 };
 
 struct SparseMaps {
@@ -115,8 +124,14 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, ui
                  "r"(src), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void bulk_wait_read_1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+// Prefetch a 4-D tiled box into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -167,8 +182,8 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < L::kNumBars; ++i) {
             const bool by128 = i == L::kBarPds || i == L::kBarDkvFree || i == L::kBarDkvFree + 1 ||
-                               i == L::kBarItemDone || i == L::kBarDQRead;
-            mbar_init(bar(i), i < NB ? 64 : (by128 ? 128 : 1));
+                               i == L::kBarItemDone || i == L::kBarDQRead || i == L::kBarStageFree;
+            mbar_init(bar(i), i == L::kBarKV ? 64 : (by128 ? 128 : 1));
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -185,37 +200,35 @@ __global__ void __launch_bounds__(kSpThreads, 1)
 
     if (warp == 4 || warp == 5) {
         // ------------------------------------------------------------ row gather
-        const int gt = tid - 128;                            // entries gt and gt + 64 of the item
-        const uint32_t dst = sbase + L::kKV + gt * 128;      // (the same swizzle phase: 64 = 0 mod 8)
+        // Thread g copies 16-byte chunk (g & 7) of rows (g >> 3) + 8 k, k < 16:
+        // every warp instruction moves four whole 128-byte row blocks.
+        const int g = tid - 128, j = g & 7, rs = g >> 3;
         int n = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < T; t += gridDim.x) {
             const TokenInfo ti = token_info(p, t);
             for (int c = 0; c < ti.nch; ++c, ++n) {
-                // the previous item's S^T, dP^T and dQ^T MMAs have read the rows
-                if (n > 0 && !(ok = mbar_wait(bar(L::kBarKVFree), (n - 1) & 1, abort_flag))) break;
-                const int r0 = entry_row(p, ti, c * kSpE + gt);
-                const int r1 = entry_row(p, ti, c * kSpE + gt + 64);
-                const uint8_t* src0 = reinterpret_cast<const uint8_t*>(
-                    p.kv + ti.b * p.kv_b + static_cast<int64_t>(r0 < 0 ? 0 : r0) * p.kv_s);
-                const uint8_t* src1 = reinterpret_cast<const uint8_t*>(
-                    p.kv + ti.b * p.kv_b + static_cast<int64_t>(r1 < 0 ? 0 : r1) * p.kv_s);
+                // the previous item's MMAs have read the rows and its dKV
+                // staging over the same region has been read by the bulk adds
+                if (n > 0 && !(ok = mbar_wait(bar(L::kBarStageFree), (n - 1) & 1, abort_flag))) break;
+                const uint8_t* src[kSpE / 8];
 #pragma unroll
-                for (int blk = 0; blk < NB; ++blk) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t o = blk * 16384 + ((j ^ (gt & 7)) << 4);
-                        cp_async16(dst + o, src0 + blk * 128 + j * 16);
-                        cp_async16(dst + 64 * 128 + o, src1 + blk * 128 + j * 16);
-                    }
-                    cp_async_commit();
+                for (int k = 0; k < kSpE / 8; ++k) {
+                    const int row = entry_row(p, ti, c * kSpE + 8 * k + rs);
+                    src[k] = reinterpret_cast<const uint8_t*>(
+                                 p.kv + ti.b * p.kv_b + static_cast<int64_t>(row < 0 ? 0 : row) * p.kv_s) +
+                             16 * j;
                 }
+                const uint32_t dst = sbase + L::kKV + rs * 128 + ((j ^ rs) << 4);   // (8k + rs) & 7 = rs
 #pragma unroll
-                for (int blk = 0; blk < NB; ++blk) {
-                    cp_async_wait(NB - 1 - blk);
-                    fence_proxy_async_smem();                // generic-proxy writes -> UMMA reads
-                    mbar_arrive(bar(L::kBarKV + blk));
-                }
+                for (int blk = 0; blk < NB; ++blk)
+#pragma unroll
+                    for (int k = 0; k < kSpE / 8; ++k)
+                        cp_async16(dst + blk * 16384 + k * 1024, src[k] + blk * 128);
+                cp_async_commit();
+                cp_async_wait(0);
+                fence_proxy_async_smem();                    // generic-proxy writes -> UMMA reads
+                mbar_arrive(bar(L::kBarKV));
             }
         }
         cp_async_wait(0);
@@ -226,22 +239,28 @@ __global__ void __launch_bounds__(kSpThreads, 1)
             tma_prefetch_desc(&maps.dout);
             int r = 0;
             bool ok = true;
-            auto load = [&](const CUtensorMap* m, int blk, const TokenInfo& ti) {
+            auto load = [&](int blk, const TokenInfo& ti) {       // Q block (and dO block) blk
                 const int s = r % kRing;
                 if (!(ok = mbar_wait(bar(L::kBarREmpty + s), ((r / kRing) & 1) ^ 1, abort_flag))) return;
-                mbar_arrive_expect_tx(bar(L::kBarRFull + s), 8192);
-                tma_load_4d(sbase + L::kRingOff + s * 8192, m, 64 * blk, 0, ti.i, ti.b,
-                            bar(L::kBarRFull + s));
+                const bool with_do = blk < L::kNBV;
+                mbar_arrive_expect_tx(bar(L::kBarRFull + s), with_do ? 16384 : 8192);
+                const uint32_t d = sbase + L::kRingOff + s * 16384;
+                tma_load_4d(d, &maps.q, 64 * blk, 0, ti.i, ti.b, bar(L::kBarRFull + s));
+                if (with_do) tma_load_4d(d + 8192, &maps.dout, 64 * blk, 0, ti.i, ti.b, bar(L::kBarRFull + s));
                 ++r;
             };
             for (int t = blockIdx.x; ok && t < T; t += gridDim.x) {
                 const TokenInfo ti = token_info(p, t);
+                if (t + static_cast<int>(gridDim.x) < T) {
+                    const int tn = t + gridDim.x, bn = tn / p.S, in = tn - bn * p.S;
+                    for (int blk = 0; blk < NB; ++blk) {
+                        tma_prefetch_l2_4d(&maps.q, 64 * blk, 0, in, bn);
+                        if (blk < L::kNBV) tma_prefetch_l2_4d(&maps.dout, 64 * blk, 0, in, bn);
+                    }
+                }
                 for (int c = 0; ok && c < ti.nch; ++c)
                     for (int pass = 0; ok && pass < 2; ++pass)       // S^T / dP^T, then dKV
-                        for (int blk = 0; ok && blk < NB; ++blk) {
-                            load(&maps.q, blk, ti);
-                            if (ok && blk < L::kNBV) load(&maps.dout, blk, ti);
-                        }
+                        for (int blk = 0; ok && blk < NB; ++blk) load(blk, ti);
             }
             if (*abort_flag) {
                 volatile int no_abort = 0;
@@ -259,14 +278,13 @@ __global__ void __launch_bounds__(kSpThreads, 1)
             const uint64_t ds_mn = smem_desc(sbase + L::kDS, 8192, 1024, kSwizzle128B);
             int n = 0, r = 0, g = 0, tk = 0;
             bool ok = true;
-            // next ring block: wait for it, return its K-major and MN-major descriptors
-            auto ring_next = [&](uint64_t* kmaj, uint64_t* mn) -> int {
+            // next ring stage: wait for it, return its shared address (Q block,
+            // then the dO block 8 KB later)
+            auto ring_next = [&](uint32_t* addr) -> int {
                 const int s = r % kRing;
                 if (!(ok = mbar_wait(bar(L::kBarRFull + s), (r / kRing) & 1, abort_flag))) return s;
                 tc_fence_after();
-                const uint32_t a = sbase + L::kRingOff + s * 8192;
-                *kmaj = smem_desc(a, 16, 1024, kSwizzle128B);
-                *mn = smem_desc(a, 8192, 1024, kSwizzle128B);
+                *addr = sbase + L::kRingOff + s * 16384;
                 ++r;
                 return s;
             };
@@ -280,27 +298,25 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                     if (n > 0 && !(ok = mbar_wait(bar(L::kBarItemDone), (n - 1) & 1, abort_flag))) break;
                     tc_fence_after();
                     // S^T and dP^T over the 64-column blocks of the gathered rows
+                    if (!(ok = mbar_wait(bar(L::kBarKV), n & 1, abort_flag))) break;
                     for (int blk = 0; ok && blk < NB; ++blk) {
-                        if (!(ok = mbar_wait(bar(L::kBarKV + blk), n & 1, abort_flag))) break;
-                        tc_fence_after();
                         const uint64_t a = smem_desc(sbase + L::kKV + blk * 16384, 16, 1024, kSwizzle128B);
-                        uint64_t bk, bm;
-                        int s = ring_next(&bk, &bm);
+                        uint32_t ra;
+                        const int s = ring_next(&ra);
                         if (!ok) break;
+                        const uint64_t bq = smem_desc(ra, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(ra + 8192, 16, 1024, kSwizzle128B);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tmem + L::kColS, desc_add(a, 32 * kk), desc_add(bk, 32 * kk), id_s,
+                            mma_ss(tmem + L::kColS, desc_add(a, 32 * kk), desc_add(bq, 32 * kk), id_s,
                                    (blk | kk) != 0);
-                        mma_commit(bar(L::kBarREmpty + s));
                         if (blk < L::kNBV) {
-                            s = ring_next(&bk, &bm);
-                            if (!ok) break;
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tmem + L::kColDP, desc_add(a, 32 * kk), desc_add(bk, 32 * kk), id_s,
+                                mma_ss(tmem + L::kColDP, desc_add(a, 32 * kk), desc_add(bd, 32 * kk), id_s,
                                        (blk | kk) != 0);
-                            mma_commit(bar(L::kBarREmpty + s));
                         }
+                        mma_commit(bar(L::kBarREmpty + s));
                     }
                     if (!ok) break;
                     mma_commit(bar(L::kBarSdp));
@@ -330,21 +346,20 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                             break;
                         tc_fence_after();
                         const uint32_t dkv = tmem + (buf ? L::kColDP : L::kColKV0);
-                        uint64_t bk, bm;
-                        int s = ring_next(&bk, &bm);
+                        uint32_t ra;
+                        const int s = ring_next(&ra);
                         if (!ok) break;
+                        const uint64_t bq = smem_desc(ra, 8192, 1024, kSwizzle128B);        // MN-major
+                        const uint64_t bd = smem_desc(ra + 8192, 8192, 1024, kSwizzle128B);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ts(dkv, tmem + L::kColS + 32 + 8 * kk, desc_add(bm, 2048 * kk), id_kv, kk > 0);
-                        mma_commit(bar(L::kBarREmpty + s));
+                            mma_ts(dkv, tmem + L::kColS + 32 + 8 * kk, desc_add(bq, 2048 * kk), id_kv, kk > 0);
                         if (j < L::kNBV) {
-                            s = ring_next(&bk, &bm);
-                            if (!ok) break;
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_ts(dkv, tmem + L::kColS + 8 * kk, desc_add(bm, 2048 * kk), id_kv, 1);
-                            mma_commit(bar(L::kBarREmpty + s));
+                                mma_ts(dkv, tmem + L::kColS + 8 * kk, desc_add(bd, 2048 * kk), id_kv, 1);
                         }
+                        mma_commit(bar(L::kBarREmpty + s));
                         mma_commit(bar(L::kBarDkvFull + buf));
                     }
                 }
@@ -368,8 +383,8 @@ __global__ void __launch_bounds__(kSpThreads, 1)
             // the token's 64 lse and Delta values: the same address in every
             // lane (L1 broadcasts); no block-level barrier, so that a warp that
             // unwinds early cannot leave the others waiting
-            const float* lse_t = p.lse + static_cast<int64_t>(t) * kSpH;
-            const float* delta_t = p.delta + static_cast<int64_t>(t) * kSpH;
+            const float4* lse_t = reinterpret_cast<const float4*>(p.lse + static_cast<int64_t>(t) * kSpH);
+            const float4* delta_t = reinterpret_cast<const float4*>(p.delta + static_cast<int64_t>(t) * kSpH);
             for (int c = 0; ok && c < ti.nch; ++c, ++n) {
                 const int row = entry_row(p, ti, c * kSpE + key);
                 const bool valid = row >= 0;
@@ -385,10 +400,16 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                     uint32_t x[kSpH];
                     tmem_ld32x2(tl + L::kColS, x, tl + L::kColS + 32, x + 32);
 #pragma unroll
-                    for (int h = 0; h < kSpH; ++h)
-                        P[h] = valid ? ex2(fminf(fmaf(__uint_as_float(x[h]), c2, -__ldg(lse_t + h) * kLog2e),
-                                                 0.f))
-                                     : 0.f;
+                    for (int h4 = 0; h4 < kSpH / 4; ++h4) {
+                        const float4 l = __ldg(lse_t + h4);
+                        const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int h = 4 * h4 + u;
+                            P[h] = valid ? ex2(fminf(fmaf(__uint_as_float(x[h]), c2, -lv[u] * kLog2e), 0.f))
+                                         : 0.f;
+                        }
+                    }
                     uint32_t pk[32];
 #pragma unroll
                     for (int h = 0; h < 32; ++h) pk[h] = pack2<F16>(P[2 * h], P[2 * h + 1]);
@@ -403,12 +424,13 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                     tmem_ld32(tl + L::kColDP + 32 * half, y);
                     uint32_t dk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int h = 32 * half + 2 * e;
-                        const float d0 = P[h] * (__uint_as_float(y[2 * e]) - __ldg(delta_t + h)) * p.scale;
-                        const float d1 =
-                            P[h + 1] * (__uint_as_float(y[2 * e + 1]) - __ldg(delta_t + h + 1)) * p.scale;
-                        dk[e] = pack2<F16>(d0, d1);
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 dl = __ldg(delta_t + 8 * half + e4);
+                        const int h = 32 * half + 4 * e4;
+                        dk[2 * e4] = pack2<F16>(P[h] * (__uint_as_float(y[4 * e4]) - dl.x) * p.scale,
+                                                P[h + 1] * (__uint_as_float(y[4 * e4 + 1]) - dl.y) * p.scale);
+                        dk[2 * e4 + 1] = pack2<F16>(P[h + 2] * (__uint_as_float(y[4 * e4 + 2]) - dl.z) * p.scale,
+                                                    P[h + 3] * (__uint_as_float(y[4 * e4 + 3]) - dl.w) * p.scale);
                     }
                     tmem_st16(tl + L::kColS + 32 + 16 * half, dk);
 #pragma unroll
@@ -422,8 +444,10 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bar(L::kBarPds));
-                // dKV chunks: read out, stage the row, bulk fp32 add into dkv_acc[row]
+                // dKV chunks: read out and stage the row in 32-column pieces; a
+                // bulk fp32 add of each half row (NB pieces) into dkv_acc[row]
                 float* acc_row = p.dkv_acc + (static_cast<int64_t>(ti.b) * p.Skv + (valid ? row : 0)) * p.Dqk;
+                const uint32_t st_row = sbase + L::kKV + key * L::kStRow;
                 for (int j = 0; j < NB; ++j, ++g) {
                     const int buf = g & 1, u = g >> 1;
                     ok = mbar_wait(bar(L::kBarDkvFull + buf), u & 1, abort_flag);
@@ -437,21 +461,35 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                     tmem_ld32x2(tl + col, x, tl + col + 32, x + 32);
                     tc_fence_before();
                     mbar_arrive(bar(L::kBarDkvFree + buf));
+                    if (j == 0) {
+                        // dQ^T's MMAs have read the gathered rows: the region is staging now
+                        ok = mbar_wait(bar(L::kBarKVFree), n & 1, abort_flag);
+                        if (!__all_sync(0xffffffffu, ok)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     if (valid) {
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
-                            const uint32_t srow = sbase + L::kStage + (warp * 2 + half) * kStageSlot +
-                                                  lane * kStageRow;
-                            bulk_wait_read_1();              // this slot's previous add has read it
+                            const int pc = 2 * j + half, q = pc % NB;
+                            if (pc == NB) bulk_wait_read_0();        // the first half row has been read
 #pragma unroll
                             for (int q4 = 0; q4 < 8; ++q4)
-                                sts128(srow + 16 * q4, x[32 * half + 4 * q4], x[32 * half + 4 * q4 + 1],
-                                       x[32 * half + 4 * q4 + 2], x[32 * half + 4 * q4 + 3]);
-                            fence_proxy_async_smem();
-                            bulk_reduce_add_f32(acc_row + 64 * j + 32 * half, srow, 128);
-                            bulk_commit();
+                                sts128(st_row + 128 * q + 16 * q4, x[32 * half + 4 * q4],
+                                       x[32 * half + 4 * q4 + 1], x[32 * half + 4 * q4 + 2],
+                                       x[32 * half + 4 * q4 + 3]);
+                            if (q == NB - 1) {
+                                fence_proxy_async_smem();
+                                bulk_reduce_add_f32(acc_row + (pc / NB) * NB * 32, st_row, NB * 128);
+                                bulk_commit();
+                            }
                         }
                     }
+                }
+                if (ok) {
+                    bulk_wait_read_0();
+                    mbar_arrive(bar(L::kBarStageFree));
                 }
                 if (!ok) break;
                 mbar_arrive(bar(L::kBarItemDone));
