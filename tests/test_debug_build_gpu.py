@@ -91,9 +91,33 @@ def test_checked_build_score_recompute_matches_product_build(checked_lib):
         assert torch.equal(a, b)
 
 
+def _sparse_inputs(S=8, Skv=600, K=512, seed=36, length=False):
+    c = W.dsa_case(B=1, S=S, Skv=Skv, D=576, K=K, seed=seed, length=length)
+    d = {k: (None if v is None else v.cuda()) for k, v in c.items()}
+    d["out"] = torch.randn(1, S, 64, 512, device="cuda").bfloat16()
+    d["lse"] = torch.randn(1, S, 64, device="cuda") + 8.0
+    return d
+
+
+def test_checked_build_sparse_bwd_matches_product_build(checked_lib):
+    from softmax_attention_numerics_gb300 import _lib, attn_sparse_bwd, get_error
+    d = _sparse_inputs(S=40, Skv=700, K=300, length=True)
+    args = (d["q"], d["kv"], d["out"], d["dout"], d["lse"], d["topk_idxs"])
+    kw = dict(topk_length=d["topk_length"], attn_sink=d["attn_sink"], scale=0.04)
+    ref = attn_sparse_bwd(*args, **kw)
+    with _lib.use_library(checked_lib):
+        got = attn_sparse_bwd(*args, **kw)
+        torch.cuda.synchronize()
+        assert get_error() == 0
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[2], ref[2])       # dq, d_sink
+    assert torch.allclose(got[1].float(), ref[1].float(), rtol=2e-2, atol=1e-3)   # fp32 add order
+
+
 # (kernel, iteration of its MMA issuer's loop): 1 forward, 2 backward main,
-# 3 deterministic dQ, 4 fp8 forward, 5 score recompute (the loop runs over heads).
-STALLS = [(1, 0), (1, 3), (2, 0), (2, 5), (3, 0), (3, 2), (4, 0), (4, 2), (5, 0), (5, 3)]
+# 3 deterministic dQ, 4 fp8 forward, 5 score recompute (the loop runs over heads),
+# 6 sparse backward (the loop runs over work items: token 0 has four of them).
+STALLS = [(1, 0), (1, 3), (2, 0), (2, 5), (3, 0), (3, 2), (4, 0), (4, 2), (5, 0), (5, 3),
+          (6, 0), (6, 3)]
 
 
 def _stalled_call(kernel):
@@ -101,6 +125,12 @@ def _stalled_call(kernel):
     (0, 0, 0) runs more than three iterations of its loop."""
     from softmax_attention_numerics_gb300 import attn_bwd, attn_fwd, attn_fwd_fp8
     from softmax_attention_numerics_gb300 import attn_score_recompute
+    if kernel == 6:
+        from softmax_attention_numerics_gb300 import attn_sparse_bwd
+        d = _sparse_inputs()
+        attn_sparse_bwd(d["q"], d["kv"], d["out"], d["dout"], d["lse"], d["topk_idxs"],
+                        attn_sink=d["attn_sink"], scale=0.04)
+        return
     if kernel == 5:
         q, k, _, _ = (t.cuda() for t in W.dense_qkvdo(1, 300, 300, 8, 2, 128, seed=35))
         lse = torch.zeros(1, 8, 300, device="cuda")
