@@ -293,11 +293,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             } else {
                 // full tile, no mask: the max of the raw scores, scaled once
-                // (x stays unscaled; P below folds the scale into one FMA)
-                tmem_ld128(tS, reinterpret_cast<uint32_t*>(x));
+                // (x stays unscaled; P below folds the scale into one FMA).  The
+                // second half of the row is still loading from TMEM while the
+                // max of the first half runs.
+                uint32_t* xu = reinterpret_cast<uint32_t*>(x);
+                tmem_ld32x2(tS, xu, tS + 32, xu + 32);
+                tmem_ld64_nowait(tS + 64, xu + 64);
                 float mr = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < kTile; ++c) mr = fmaxf(mr, x[c]);
+                for (int c = 0; c < kTile / 2; ++c) mr = fmaxf(mr, x[c]);
+                tmem_wait_ld_regs64(xu + 64);
+#pragma unroll
+                for (int c = kTile / 2; c < kTile; ++c) mr = fmaxf(mr, x[c]);
                 if (p.scale_log2 > 0.f) {
                     mt = mr * p.scale_log2;
                 } else {
