@@ -393,7 +393,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     uint32_t pk[16], dk[16];
                     // Phase A: P^T = exp2(min(x - lse2, 0)), kept in sv as fp32 and
                     // packed into pk; hidden entries are exactly 0.
-                    if (!pred && !kMask) {
+                    if (!kSplit && !pred && !kMask) {
+                        // one pass: P^T and dS^T together (dP^T is already loaded)
+                        const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+                        float4 lv = lds128(va), dl = lds128(va + 512), lvn, dln;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            if ((e & 3) == 0 && e + 4 < 32) {
+                                lvn = lds128(va + 4 * e + 16);
+                                dln = lds128(va + 512 + 4 * e + 16);
+                            }
+                            const float2 l2 = (e & 2) ? make_float2(lv.z, lv.w) : make_float2(lv.x, lv.y);
+                            const float2 nd2 = (e & 2) ? make_float2(dl.z, dl.w) : make_float2(dl.x, dl.y);
+                            const float2 x2 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                    c2, l2);
+                            const float p0 = ex2(fminf(x2.x, 0.f));
+                            const float p1 = ex2(fminf(x2.y, 0.f));
+                            const float2 d2 = fadd2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                                    nd2);
+                            const float2 ds2 = fmul2(make_float2(p0, p1), d2);
+                            pk[e >> 1] = pack2<F16>(p0, p1);
+                            dk[e >> 1] = pack2<F16>(ds2.x, ds2.y);
+                            if ((e & 3) == 2) {
+                                lv = lvn;
+                                dl = dln;
+                            }
+                        }
+                    } else if (!pred && !kMask) {
                         const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
                         float4 lv = lds128(va), lvn;
 #pragma unroll
@@ -458,7 +484,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tmem_ld32(tDP + 32 * c, dv);
                     }
                     // Phase B: dS^T = P^T o (dP^T - Delta); hidden entries stay exactly 0.
-                    if (!pred && !kMask) {
+                    if (!kSplit && !pred && !kMask) {
+                        // done in the one-pass loop above
+                    } else if (!pred && !kMask) {
                         float4 dl = lds128(va + 512), dln;
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
