@@ -230,9 +230,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(L::kBarSFree + buf));            // the values are in registers
             if (full && row_in) {
+                // packed pairs: one FMA and one add per two terms
+                const float2 c2 = make_float2(c, c), nl2 = make_float2(nl, nl);
 #pragma unroll
-                for (int e = 0; e < 64; ++e)
-                    acc[e] += ex2(fminf(fmaf(__uint_as_float(v[e]), c, nl), kScoreClamp));
+                for (int e = 0; e < 64; e += 2) {
+                    const float2 x2 = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2, nl2);
+                    const float2 t2 = make_float2(ex2(fminf(x2.x, kScoreClamp)), ex2(fminf(x2.y, kScoreClamp)));
+                    const float2 a2 = fadd2(make_float2(acc[e], acc[e + 1]), t2);
+                    acc[e] = a2.x;
+                    acc[e + 1] = a2.y;
+                }
             } else {
 #pragma unroll
                 for (int e = 0; e < 64; ++e) {
