@@ -30,7 +30,10 @@ template <int D>
 struct DqLayout {
     static constexpr int kBlocks = D / 64;
     static constexpr int kTileBytes = kT * D * 2;
-    static constexpr int kStages = (D == 128) ? 3 : 6;     // K/V ring
+    // K/V ring.  At iteration j the issuer needs K_j (until dQ_j), K_{j+1} and
+    // V_{j+1} resident at once (dP_{j+1} is issued before dQ_j), plus a slot
+    // being filled: at least four slots.
+    static constexpr int kStages = (D == 128) ? 4 : 6;
     static constexpr int kQ = 0;
     static constexpr int kDO = kTileBytes;
     static constexpr int kKV = 2 * kTileBytes;
@@ -44,7 +47,8 @@ struct DqLayout {
     static constexpr int kBarDQDone = kBarDSReady + 1;        // [2]: dQ_j read S buffer j&1
     static constexpr int kBarFinal = kBarDQDone + 2;
     static constexpr int kBarDrain = kBarFinal + 1;
-    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kBarDPRead = kBarDrain + 1;          // dP_j in registers (256)
+    static constexpr int kNumBars = kBarDPRead + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     static constexpr uint32_t kTmemCols = 512;
@@ -83,7 +87,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < L::kNumBars; ++i)
-            mbar_init(bar(i), i == L::kBarDSReady ? 2 * kT : 1);
+            mbar_init(bar(i), (i == L::kBarDSReady || i == L::kBarDPRead) ? 2 * kT : 1);
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -187,8 +191,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     tc_fence_after();
                     issue_s(j + 1);
                     mma_commit(bar(L::kBarSFull + ((j + 1) & 1)));
+                    // dP_{j+1} as soon as the compute warps hold dP_j in registers
+                    // (it runs while they work on tile j, ahead of dQ_j)
+                    if (!(ok = mbar_wait(bar(L::kBarDPRead), j & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait(bar(L::kBarKVFull + stage(2 * j + 3)), par(2 * j + 3),
+                                         abort_flag)))
+                        break;
+                    tc_fence_after();
+                    issue_dp(j + 1);
+                    mma_commit(bar(L::kBarDPFull));
+                    mma_commit(bar(L::kBarKVEmpty + stage(2 * j + 3)));   // V_{j+1} consumed
                 }
-                // dS_j written (and dP_j fully read) by the compute warps.
+                // dS_j written by the compute warps.
                 if (!(ok = mbar_wait(bar(L::kBarDSReady), j & 1, abort_flag))) break;
                 tc_fence_after();
                 {
@@ -202,14 +216,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 }
                 mma_commit(bar(L::kBarDQDone + (j & 1)));
                 mma_commit(bar(L::kBarKVEmpty + stage(2 * j)));     // K_j consumed
-                if (next) {
-                    if (!(ok = mbar_wait(bar(L::kBarKVFull + stage(2 * j + 3)), par(2 * j + 3),
-                                         abort_flag)))
-                        break;
-                    issue_dp(j + 1);
-                    mma_commit(bar(L::kBarDPFull));
-                    mma_commit(bar(L::kBarKVEmpty + stage(2 * j + 3)));   // V_{j+1} consumed
-                }
             }
             mma_commit(bar(L::kBarFinal));
             if (!ok) {
@@ -260,10 +266,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 tmem_wait_st();
             }
             const int jmax = p.causal ? min(si.len_k, i + 1) : si.len_k;   // keys < jmax visible
-#pragma unroll 1
-            for (int c = 2 * hq; c < 2 * hq + 2; ++c) {
-                uint32_t sv[32], dv[32];
-                tmem_ld32x2(tS + 32 * c, sv, tDP + 32 * c, dv);
+            // this warp's half of dP_j to registers first, so that dP_{j+1} can
+            // start on the tensor cores while the tile is worked on
+            uint32_t dph[64];
+            tmem_ld32x2(tDP + 64 * hq, dph, tDP + 64 * hq + 32, dph + 32);
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDPRead));
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * hq + cc;
+                uint32_t sv[32];
+                const uint32_t* dv = dph + 32 * cc;
+                tmem_ld32(tS + 32 * c, sv);
                 uint32_t pk[16];
                 if (!pred && !has_mask) {
                     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
