@@ -32,8 +32,10 @@ struct DqLayout {
     static constexpr int kTileBytes = kT * D * 2;
     // K/V ring.  At iteration j the issuer needs K_j (until dQ_j), K_{j+1} and
     // V_{j+1} resident at once (dP_{j+1} is issued before dQ_j), plus a slot
-    // being filled: at least four slots.
-    static constexpr int kStages = (D == 128) ? 4 : 6;
+    // being filled: at least four slots.  With five, K_{j+2} goes into the
+    // slot V_{j-1} left (free early) instead of K_j's, so its load is not
+    // held until dQ_j completes.
+    static constexpr int kStages = (D == 128) ? 5 : 6;
     static constexpr int kQ = 0;
     static constexpr int kDO = kTileBytes;
     static constexpr int kKV = 2 * kTileBytes;
@@ -51,6 +53,7 @@ struct DqLayout {
     static constexpr int kNumBars = kBarDPRead + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
+    static_assert(kBytes <= 232448, "shared memory");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColDP = 256, kColDQ = 384;
 };
