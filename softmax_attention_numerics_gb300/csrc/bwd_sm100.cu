@@ -193,13 +193,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int issued = 0;
         for (int it = 0; it < n_iter; ++it) {
             const int s = it & 1, r = it >> 1;
+            int h, m0;
+            iter_tile(it, &h, &m0);
+            // this tile's -lse2 / -Delta to registers before the wait for the
+            // stage, so that their latency overlaps it
+            float nlv[4], ndv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = m0 + 4 * lane + e;
+                const int64_t li = b * p.lse_b + h * p.lse_h + row_base + i;
+                const bool in = i < si.len_q;
+                nlv[e] = in ? -p.lse2[li] : 0.f;     // both stored negated
+                ndv[e] = in ? -p.delta[li] : 0.f;
+            }
             ok = mbar_wait(bar(L::kBarQEmpty + s), (r & 1) ^ 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
-            int h, m0;
-            iter_tile(it, &h, &m0);
             // every query tile starts inside the sequence, every head inside the group
             if (lane == 0 && dbg_check(m0 < si.len_q && h >= hk * p.G && h < (hk + 1) * p.G, p.err)) {
                 mbar_arrive_expect_tx(bar(L::kBarQFull + s), 2 * L::kTileBytes);
@@ -213,12 +224,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int q = 4 * lane + e;
-                const int i = m0 + q;
-                const int64_t li = b * p.lse_b + h * p.lse_h + row_base + i;
-                const bool in = i < si.len_q;
-                vec[s * 256 + q] = in ? -p.lse2[li] : 0.f;     // both stored negated
-                vec[s * 256 + 128 + q] = in ? -p.delta[li] : 0.f;
+                vec[s * 256 + 4 * lane + e] = nlv[e];
+                vec[s * 256 + 128 + 4 * lane + e] = ndv[e];
             }
             mbar_arrive(bar(L::kBarQFull + s));
             issued = it + 1;
