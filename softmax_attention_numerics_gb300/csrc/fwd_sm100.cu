@@ -31,6 +31,11 @@
 namespace attn {
 namespace {
 
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
 using namespace sm100;
 
 constexpr int kFwdThreads = 320;
@@ -336,22 +341,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
             const float2 nms2 = make_float2(-ms, -ms);
             const float2 c2 = raw ? make_float2(p.scale_log2, p.scale_log2) : make_float2(1.f, 1.f);
+            // P = exp2(min(x - m_ref, 8)).  The clamp cannot bind on a row whose tile
+            // max is within 8 of m_ref (the lazy test passed) or that rescaled
+            // (m_ref >= the tile max); when that holds for the whole warp with a
+            // margin for rounding, the per-element min is skipped.
+            auto exps = [&](auto clamp_tag) {
+                constexpr bool kClamp = decltype(clamp_tag)::value;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    // x - m_ref in one packed FMA (the scale folded in when x is raw)
-                    const float2 d2 = ffma2(make_float2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), c2, nms2);
-                    float2 p2;
-                    p2.x = ex2(fminf(d2.x, kLazyTau));
-                    p2.y = ex2(fminf(d2.y, kLazyTau));
-                    l2 = fadd2(l2, p2);
-                    pk[e] = pack2<F16>(p2.x, p2.y);
-                    lr2 = fadd2(lr2, unpack2<F16>(pk[e]));
+                    for (int e = 0; e < 16; ++e) {
+                        // x - m_ref in one packed FMA (the scale folded in when x is raw)
+                        const float2 d2 = ffma2(make_float2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), c2, nms2);
+                        float2 p2;
+                        p2.x = ex2(kClamp ? fminf(d2.x, kLazyTau) : d2.x);
+                        p2.y = ex2(kClamp ? fminf(d2.y, kLazyTau) : d2.y);
+                        l2 = fadd2(l2, p2);
+                        pk[e] = pack2<F16>(p2.x, p2.y);
+                        lr2 = fadd2(lr2, unpack2<F16>(pk[e]));
+                    }
+                    tmem_st16(tS + 16 * c, pk);
                 }
-                tmem_st16(tS + 16 * c, pk);
-            }
+            };
+            if (__all_sync(0xffffffffu, mt - ms <= kLazyTau - 0.015625f))
+                exps(BoolTag<false>{});
+            else
+                exps(BoolTag<true>{});
             // Rescale O_t in TMEM (its previous MMA has completed: the commit that
             // signalled S_t(j) was issued after it).
             if (__any_sync(0xffffffffu, corr != 1.f)) {
