@@ -27,6 +27,11 @@
 namespace attn {
 namespace {
 
+template <bool B>
+struct F8Tag {
+    static constexpr bool value = B;
+};
+
 using namespace sm100;
 
 constexpr int kF8Threads = 320;
@@ -288,23 +293,35 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             }
             const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
             // P^ row: 128 E4M3 = 8 chunks of 16 bytes, chunk c at (c ^ (row & 7)) * 16.
+            // p = exp2(min(x - m_ref, 8)); x - m_ref <= m_tile - m_ref exactly (x is
+            // the scaled score itself), so when every row of the warp has
+            // m_tile - m_ref <= 8 the per-element min is skipped.
+            auto exps = [&](auto clamp_tag) {
+                constexpr bool kClamp = decltype(clamp_tag)::value;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t w[4];
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t w[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int k0 = 16 * c + 4 * e;
-                    float pv[4];
+                    for (int e = 0; e < 4; ++e) {
+                        const int k0 = 16 * c + 4 * e;
+                        float pv[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) pv[u] = ex2(fminf(x[k0 + u] - ms, 8.f));
-                    l2 = fadd2(l2, make_float2(pv[0] + pv[2], pv[1] + pv[3]));
-                    const uint32_t lo = pack_e4m3x2(pv[0], pv[1]), hi = pack_e4m3x2(pv[2], pv[3]);
-                    const float2 a = unpack_e4m3x2(lo), bq = unpack_e4m3x2(hi);
-                    lr2 = fadd2(lr2, make_float2(a.x + bq.x, a.y + bq.y));
-                    w[e] = lo | (hi << 16);
+                        for (int u = 0; u < 4; ++u)
+                            pv[u] = ex2(kClamp ? fminf(x[k0 + u] - ms, 8.f) : x[k0 + u] - ms);
+                        l2 = fadd2(l2, make_float2(pv[0] + pv[2], pv[1] + pv[3]));
+                        const uint32_t lo = pack_e4m3x2(pv[0], pv[1]), hi = pack_e4m3x2(pv[2], pv[3]);
+                        const float2 a = unpack_e4m3x2(lo), bq = unpack_e4m3x2(hi);
+                        lr2 = fadd2(lr2, make_float2(a.x + bq.x, a.y + bq.y));
+                        w[e] = lo | (hi << 16);
+                    }
+                    *reinterpret_cast<uint4*>(prow + ((c ^ (r_local & 7)) << 4)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                *reinterpret_cast<uint4*>(prow + ((c ^ (r_local & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+            };
+            if (__all_sync(0xffffffffu, mt - ms <= 8.f))
+                exps(F8Tag<false>{});
+            else
+                exps(F8Tag<true>{});
             fence_proxy_async_smem();   // generic stores of P^ -> tensor core reads
             if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
