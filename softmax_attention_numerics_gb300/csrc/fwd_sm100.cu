@@ -308,8 +308,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                 for (int c = 0; c < kTile / 2; ++c) mr = fmaxf(mr, x[c]);
                 tmem_wait_ld_regs64(xu + 64);
+                if constexpr (D == 64) {
+                    // two chains for the half on the critical path (measured faster at
+                    // D = 64, slower at D = 128)
+                    float mr1 = -INFINITY;
 #pragma unroll
-                for (int c = kTile / 2; c < kTile; ++c) mr = fmaxf(mr, x[c]);
+                    for (int c = kTile / 2; c < kTile; c += 2) {
+                        mr = fmaxf(mr, x[c]);
+                        mr1 = fmaxf(mr1, x[c + 1]);
+                    }
+                    mr = fmaxf(mr, mr1);
+                } else {
+#pragma unroll
+                    for (int c = kTile / 2; c < kTile; ++c) mr = fmaxf(mr, x[c]);
+                }
                 if (p.scale_log2 > 0.f) {
                     mt = mr * p.scale_log2;
                 } else {
