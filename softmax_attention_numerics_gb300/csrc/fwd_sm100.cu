@@ -48,7 +48,12 @@ struct FwdLayout {
     static constexpr int kStages = (D == 128) ? 4 : 6;      // K/V ring depth
     static constexpr int kQ = 0;                            // Q0, Q1
     static constexpr int kKV = 2 * kTileBytes;
-    static constexpr int kBar = kKV + kStages * kTileBytes;
+    // D = 64: O gets 16 more columns from a 128-row block of ones appended to
+    // V in the P V product, so O's column 64 is the sum of the rounded p (the
+    // softmax then does not add them up itself).  TMEM has room for it there.
+    static constexpr bool kOnesCol = (D == 64);
+    static constexpr int kOnes = kKV + kStages * kTileBytes;   // one 128 x 64 swizzled atom of ones
+    static constexpr int kBar = kOnes + (kOnesCol ? 16384 : 0);
     // barrier slots (8 bytes each)
     static constexpr int kBarQ = 0;
     static constexpr int kBarKVFull = 1;
@@ -61,7 +66,10 @@ struct FwdLayout {
     static constexpr int kMisc = kBar + kNumBars * 8;         // tmem base, abort flag
     static constexpr int kBytes = kMisc + 16 + 1024;          // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+    static constexpr int kNO = kOnesCol ? D + 16 : D;         // N of the P V product
+    static constexpr int kOStride = kOnesCol ? D + 32 : D;    // O columns, 32-aligned
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + kOStride;
+    static_assert(kColO1 + kOStride <= kTmemCols, "TMEM columns");
 };
 
 struct FwdMaps {
@@ -99,6 +107,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     const int n_all = max(n_t[0], n_t[1]);
 
+    if constexpr (L::kOnesCol) {
+        // the block of ones (bf16 0x3f80 or fp16 0x3c00 in every element)
+        const uint32_t one2 = F16 ? 0x3c003c00u : 0x3f803f80u;
+        uint4* ones = reinterpret_cast<uint4*>(smem + L::kOnes);
+        for (int k = tid; k < 16384 / 16; k += kFwdThreads) ones[k] = make_uint4(one2, one2, one2, one2);
+        fence_proxy_async_smem();              // generic stores -> tensor core reads
+    }
     if (tid == 0) {
         for (int i = 0; i < L::kNumBars; ++i) {
             uint32_t cnt = 1;
@@ -166,7 +181,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // ------------------------------------------------------------ UMMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_f16kind(128, 128, 0, 0, F16);
-            constexpr uint32_t idesc_pv = idesc_f16kind(128, D, 0, 1, F16);
+            constexpr uint32_t idesc_pv = idesc_f16kind(128, L::kNO, 0, 1, F16);
             const uint32_t colS[2] = {L::kColS0, L::kColS1};
             const uint32_t colO[2] = {L::kColO0, L::kColO1};
             auto kv_stage = [&](int li) { return li % L::kStages; };
@@ -185,7 +200,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             };
             auto issue_pv = [&](int t, int j) {
                 const int s = kv_stage(2 * j + 1);
-                const uint64_t vd = smem_desc(sbase + L::kKV + s * L::kTileBytes, 16384, 1024, kSwizzle128B);
+                const uint32_t va = sbase + L::kKV + s * L::kTileBytes;
+                // MN-major V: with the ones block, its 64-column atom at LBO after V's
+                const uint32_t lbo = L::kOnesCol ? static_cast<uint32_t>(L::kOnes - (L::kKV + s * L::kTileBytes))
+                                                 : 16384u;
+                const uint64_t vd = smem_desc(va, lbo, 1024, kSwizzle128B);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8, desc_add(vd, kk * 2048), idesc_pv,
@@ -371,7 +390,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         p2.y = ex2(kClamp ? fminf(d2.y, kLazyTau) : d2.y);
                         l2 = fadd2(l2, p2);
                         pk[e] = pack2<F16>(p2.x, p2.y);
-                        lr2 = fadd2(lr2, unpack2<F16>(pk[e]));
+                        if constexpr (!L::kOnesCol) lr2 = fadd2(lr2, unpack2<F16>(pk[e]));
                     }
                     tmem_st16(tS + 16 * c, pk);
                 }
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             // signalled S_t(j) was issued after it).
             if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < L::kOStride / 32; ++c) {    // the sum column too
                     uint32_t o[32];
                     tmem_ld32(tO + 32 * c, o);
 #pragma unroll
@@ -409,7 +428,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (ok) {
             // Normalise by the rounded sum: out stays an exact weighted mean of V
             // even when the lazy reference max lags (largest weight up to 2^8).
-            const float l = l2.x + l2.y, lr = lr2.x + lr2.y;
+            const float l = l2.x + l2.y;
+            float lr = lr2.x + lr2.y;
+            if constexpr (L::kOnesCol) {
+                lr = 0.f;
+                if (n_mine > 0) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + D, o);              // column D: sum of the rounded p
+                    lr = __uint_as_float(o[0]);
+                }
+            }
             const float inv = lr > 0.f ? 1.0f / lr : 0.f;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
