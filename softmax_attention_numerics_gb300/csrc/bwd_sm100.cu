@@ -53,12 +53,20 @@ struct BwdLayout {
     static constexpr int kV = kTileBytes;
     static constexpr int kQ = 2 * kTileBytes;           // 2 stages
     static constexpr int kDO = 4 * kTileBytes;          // 2 stages
-    static constexpr int kDS = 6 * kTileBytes;          // dS as [128 keys][128 q] bf16
-    static constexpr int kVec = kDS + kT * kT * 2;      // lse2[2][128], delta[2][128]
+    // D = 64 (kDefer): the dV/dK/dQ products have N = 64 and run at half rate,
+    // so dQ_i leaves the chain: S^T/dP^T of the next tile are issued ahead of
+    // it, dQ has TMEM columns of its own, dS is double-buffered, and dQ_i is
+    // read out after the next tile's P/dS into an fp32 staging tile of its own.
+    static constexpr bool kDefer = (D == 64);
+    static constexpr int kDS = 6 * kTileBytes;          // dS as [128 keys][128 q] bf16 ([2] if kDefer)
+    static constexpr int kDSBytes = kT * kT * 2;
+    static constexpr int kDQS = kDS + (kDefer ? 2 : 1) * kDSBytes;   // kDefer: fp32 dQ staging
+    static constexpr int kVec = kDQS + (kDefer ? kT * D * 4 : 0);    // lse2[2][128], delta[2][128]
     static constexpr int kBar = kVec + 4 * kT * 4;
     static constexpr int kBarKV = 0;
     static constexpr int kBarQFull = 1;    // [2]
     static constexpr int kBarQEmpty = 3;   // [2]: dV/dK MMAs done + dQ reduction read the stage
+                                           // (kDefer: the MMAs alone)
     static constexpr int kBarSdp = 5;      // S^T and dP^T done
     static constexpr int kBarP = 6;        // [2]: P^T, dS^T of chunks {0, 2} / {1, 3} written
     static constexpr int kBarDQFull = 8;
@@ -67,11 +75,16 @@ struct BwdLayout {
     static constexpr int kBarAcc = 11;
     static constexpr int kBarDrain = 12;
     static constexpr int kBarDP = 13;      // dP^T done (split schedule; S^T alone on kBarSdp)
-    static constexpr int kNumBars = 14;
+    static constexpr int kBarAccRead = 14; // kDefer: the tile's dV/dK MMAs have read P^T / dS^T
+    static constexpr int kBarDQSFree = 15; // kDefer: the reduction has read the dQ staging tile
+    static constexpr int kNumBars = 16;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
+    static constexpr uint32_t kColDQ = kDefer ? 2 * D + 256 : kColDP;   // dQ: own columns or dP^T's
+    static_assert(kColDQ + D <= kTmemCols && kColDP + 128 <= kTmemCols, "TMEM columns");
+    static_assert(kBytes <= 232448, "shared memory per CTA");
 };
 
 struct BwdMaps {
@@ -112,6 +125,7 @@ template <int D, bool F16, bool kMask, bool kSplit>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_sm100_kernel(const Problem p, const __grid_constant__ BwdMaps maps, int with_dq) {
     using L = BwdLayout<D>;
+    static_assert(!(L::kDefer && kSplit), "the deferred dQ schedule has one S^T/dP^T barrier");
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int i) { return sbase + L::kBar + 8u * i; };
@@ -141,7 +155,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t cnt = 1;
             if (i == L::kBarQFull || i == L::kBarQFull + 1) cnt = 33;
             // q_empty: the MMAs' commit + the reduction issuer once the stage was read
-            if (i == L::kBarQEmpty || i == L::kBarQEmpty + 1) cnt = 2;
+            if (i == L::kBarQEmpty || i == L::kBarQEmpty + 1) cnt = L::kDefer ? 1 : 2;
             if (i == L::kBarP || i == L::kBarP + 1) cnt = 256;
             if (i == L::kBarDQRead || i == L::kBarDQStaged) cnt = 256;
             mbar_init(bar(i), cnt);
@@ -163,8 +177,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // at the same time then reduce into different dQ rows instead of all
     // hammering the same L2 lines.
     const int rot = n_iter > 0 ? static_cast<int>(blockIdx.x % n_iter) : 0;
-    // Byte offset of fp32 dQ staging block `blk` (32 columns) inside query/dO stage `s`.
+    // Byte offset of fp32 dQ staging block `blk` (32 columns): inside query/dO
+    // stage `s`, or (kDefer) in the staging tile of its own.
     auto dq_stage_off = [&](int blk, int s) {
+        if constexpr (L::kDefer) return L::kDQS + blk * 16384;
         return ((blk & 1) ? L::kDO : L::kQ) + s * L::kTileBytes + (blk >> 1) * 16384;
     };
     auto iter_tile = [&](int it, int* h, int* m0) {
@@ -248,35 +264,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t k_k = smem_desc(sbase + L::kK, 16, 1024, kSwizzle128B);
             const uint64_t v_k = smem_desc(sbase + L::kV, 16, 1024, kSwizzle128B);
             const uint64_t k_mn = smem_desc(sbase + L::kK, 16384, 1024, kSwizzle128B);
-            const uint64_t ds_mn = smem_desc(sbase + L::kDS, 16384, 1024, kSwizzle128B);
+            const uint64_t ds_mn0 = smem_desc(sbase + L::kDS, 16384, 1024, kSwizzle128B);
             bool ok = mbar_wait(bar(L::kBarKV), 0, abort_flag);
             dbg_check(L::kColDP + 128 <= L::kTmemCols && L::kColDK + D <= L::kColS, p.err);
             for (int it = 0; ok && it < n_iter; ++it) {
                 const int s = it & 1, r = it >> 1;
                 if (!(ok = dbg_stall(p.debug_stall, kStallBwd, it, bar(L::kBarDrain), abort_flag))) break;
-                if (!(ok = mbar_wait(bar(L::kBarQFull + s), r & 1, abort_flag))) break;
-                // S^T / dP^T columns are free once the previous dQ has been read out
-                // (its commit covered every earlier MMA, including dV and dK).
-                if (it > 0 && !(ok = mbar_wait(bar(L::kBarDQRead), (it - 1) & 1, abort_flag))) break;
-                tc_fence_after();
                 const uint32_t qa = sbase + L::kQ + s * L::kTileBytes;
                 const uint32_t da = sbase + L::kDO + s * L::kTileBytes;
-                const uint64_t q_k = smem_desc(qa, 16, 1024, kSwizzle128B);      // K-major
-                const uint64_t do_k = smem_desc(da, 16, 1024, kSwizzle128B);
                 const uint64_t q_mn = smem_desc(qa, 16384, 1024, kSwizzle128B);  // MN-major
                 const uint64_t do_mn = smem_desc(da, 16384, 1024, kSwizzle128B);
+                // S^T = K Q^T and dP^T = V dO^T of the tile in stage `sn` (K-major Q / dO)
+                auto issue_s = [&](int sn) {
+                    const uint64_t q_k = smem_desc(sbase + L::kQ + sn * L::kTileBytes, 16, 1024, kSwizzle128B);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tS, desc_add(k_k, off), desc_add(q_k, off), id_sdp, kk > 0);
-                }
-                if constexpr (kSplit) mma_commit(bar(L::kBarSdp));
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tS, desc_add(k_k, off), desc_add(q_k, off), id_sdp, kk > 0);
+                    }
+                };
+                auto issue_dp = [&](int sn) {
+                    const uint64_t do_k = smem_desc(sbase + L::kDO + sn * L::kTileBytes, 16, 1024, kSwizzle128B);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tDP, desc_add(v_k, off), desc_add(do_k, off), id_sdp, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tDP, desc_add(v_k, off), desc_add(do_k, off), id_sdp, kk > 0);
+                    }
+                };
+                if (!L::kDefer || it == 0) {
+                    if (!(ok = mbar_wait(bar(L::kBarQFull + s), r & 1, abort_flag))) break;
+                    // S^T / dP^T columns are free once the previous dQ has been read out
+                    // (its commit covered every earlier MMA, including dV and dK).
+                    if (it > 0 && !(ok = mbar_wait(bar(L::kBarDQRead), (it - 1) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_s(s);
+                    if constexpr (kSplit) mma_commit(bar(L::kBarSdp));
+                    issue_dp(s);
+                    mma_commit(bar(kSplit ? L::kBarDP : L::kBarSdp));
                 }
-                mma_commit(bar(kSplit ? L::kBarDP : L::kBarSdp));
                 // dV += P^T dO, dK += dS^T Q as the chunks arrive: phase 0 covers
                 // chunks 0 and 2, phase 1 chunks 1 and 3 (16 queries = 8 packed
                 // columns per step; P^T at 32c, dS^T at 32c + 16).
@@ -298,11 +323,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 if (!ok) break;
                 mma_commit(bar(L::kBarQEmpty + s));
+                {
+                    if (L::kDefer && it + 1 < n_iter) {
+                        // the next tile's dP^T at once (every compute warp read dP^T
+                        // before its arrival), its S^T once the dV/dK MMAs have read
+                        // P^T / dS^T out of the S^T columns
+                        mma_commit(bar(L::kBarAccRead));
+                        const int s1 = (it + 1) & 1;
+                        if (!(ok = mbar_wait(bar(L::kBarQFull + s1), ((it + 1) >> 1) & 1, abort_flag))) break;
+                        tc_fence_after();
+                        issue_dp(s1);
+                        if (!(ok = mbar_wait(bar(L::kBarAccRead), it & 1, abort_flag))) break;
+                        tc_fence_after();
+                        issue_s(s1);
+                        mma_commit(bar(L::kBarSdp));
+                    }
+                }
                 if (with_dq) {
-                    // dP^T's columns are free: every compute warp has read them.
+                    // dQ's columns: dP^T's (every compute warp has read them) or
+                    // (kDefer) its own, once the previous dQ has been read out
+                    if (L::kDefer && it > 0 &&
+                        !(ok = mbar_wait(bar(L::kBarDQRead), (it - 1) & 1, abort_flag)))
+                        break;
+                    tc_fence_after();
+                    const uint64_t ds_mn = desc_add(ds_mn0, L::kDefer ? (it & 1) * L::kDSBytes : 0);
 #pragma unroll
                     for (int kk = 0; kk < kT / 16; ++kk)
-                        mma_ss(tDP, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), id_dq, kk > 0);
+                        mma_ss(tmem + L::kColDQ, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), id_dq,
+                               kk > 0);
                 }
                 mma_commit(bar(L::kBarDQFull));
             }
@@ -317,7 +365,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     } else if (warp == kWarpReduce) {
         // ------------------------------------------------------------ dQ reduction issuer
         // Reduce each staged dQ_i into the fp32 workspace with bulk tensor
-        // reductions; the stage returns to the producer once they have read it.
+        // reductions; the stage (kDefer: the staging tile) is released once
+        // they have read it.
         if (lane == 0) {
             bool ok = true;
             for (int it = 0; ok && it < n_iter; ++it) {
@@ -334,7 +383,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     bulk_commit();
                     bulk_wait_read_all();          // only the committing thread may wait
                 }
-                mbar_arrive(bar(L::kBarQEmpty + s));
+                mbar_arrive(bar(L::kDefer ? L::kBarDQSFree : L::kBarQEmpty + s));
             }
         }
         __syncwarp();
@@ -350,6 +399,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tDP = tmem + lane_off + L::kColDP;
         uint8_t* ds_tile = smem + L::kDS;
         bool ok = true;
+        // dQ_i: this warp's D/2 columns for its 32 query rows, out of TMEM,
+        // then staged as fp32 in tile i's query/dO stage (every MMA that read
+        // the stage has completed once dq_full fires) or, with kDefer, in the
+        // staging tile of its own once the reduction has read dQ_{i-1} there.
+        auto read_out_dq = [&](int i) {
+            if (ok) {
+                ok = mbar_wait(bar(L::kBarDQFull), i & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            if (!ok) return;
+            tc_fence_after();
+            uint32_t dq[D / 2];
+            if (with_dq) {
+                const uint32_t src = tmem + lane_off + L::kColDQ + hq * (D / 2);
+                if constexpr (D == 128) {
+                    tmem_ld32x2(src, dq, src + 32, dq + 32);
+                } else {
+                    tmem_ld32(src, dq);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDQRead));
+            if (L::kDefer && with_dq && i > 0) {
+                ok = mbar_wait(bar(L::kBarDQSFree), (i - 1) & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) return;
+            }
+#pragma unroll
+            for (int bb = 0; bb < D / 64; ++bb) {
+                if (with_dq) {
+                    // fp32 staging: 32-column blocks of [128 rows][128 B], 16-byte
+                    // chunks swizzled; even blocks in the query stage, odd in the dO stage.
+                    const int off = dq_stage_off(hq * (D / 64) + bb, i & 1) + r * 128;
+                    // the fp32 staging row lies inside tile i's query / dO stage or
+                    // the staging tile
+                    constexpr int lo = L::kDefer ? L::kDQS : L::kQ;
+                    constexpr int hi = L::kDefer ? L::kVec : L::kDS;
+                    if (!dbg_check(off >= lo && off + 128 <= hi, p.err)) continue;
+                    uint8_t* base = smem + off;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        poison16(base + ((k ^ (r & 7)) << 4));
+                        *reinterpret_cast<uint4*>(base + ((k ^ (r & 7)) << 4)) =
+                            make_uint4(dq[32 * bb + 4 * k], dq[32 * bb + 4 * k + 1],
+                                       dq[32 * bb + 4 * k + 2], dq[32 * bb + 4 * k + 3]);
+                    }
+                }
+            }
+            if (with_dq) fence_proxy_async_smem();   // each writer: its stores -> async proxy
+            mbar_arrive(bar(L::kBarDQStaged));
+        };
         for (int it = 0; it < n_iter; ++it) {
             const int s = it & 1;
             int h, m0;
@@ -520,55 +620,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                     tmem_st16(tS + 32 * c, pk);
                     tmem_st16(tS + 32 * c + 16, dk);
-                    if (with_dq) stage_row_chunk(ds_tile, r, 32 * c, dk);
+                    if (with_dq) stage_row_chunk(ds_tile + (L::kDefer ? (it & 1) * L::kDSBytes : 0), r, 32 * c, dk);
                     tmem_wait_st();
                     fence_proxy_async_smem();      // dS in shared memory -> the dQ MMA
                     tc_fence_before();
                     mbar_arrive(bar(L::kBarP + cc));
                 }
             }
-            // dQ_i: this warp's D/2 columns for its 32 query rows, out of TMEM,
-            // then staged as fp32 in this tile's query/dO stage (every MMA that
-            // read the stage has completed once dq_full fires).
-            if (ok) {
-                ok = mbar_wait(bar(L::kBarDQFull), it & 1, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-            }
-            if (ok) {
-                tc_fence_after();
-                uint32_t dq[D / 2];
-                if (with_dq) {
-                    const uint32_t src = tDP + hq * (D / 2);
-                    if constexpr (D == 128) {
-                        tmem_ld32x2(src, dq, src + 32, dq + 32);
-                    } else {
-                        tmem_ld32(src, dq);
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(bar(L::kBarDQRead));
-#pragma unroll
-                for (int bb = 0; bb < D / 64; ++bb) {
-                    if (with_dq) {
-                        // fp32 staging: 32-column blocks of [128 rows][128 B], 16-byte
-                        // chunks swizzled; even blocks in the query stage, odd in the dO stage.
-                        const int off = dq_stage_off(hq * (D / 64) + bb, s) + r * 128;
-                        // the fp32 staging row lies inside this iteration's query / dO stage
-                        if (!dbg_check(off >= L::kQ && off + 128 <= L::kDS, p.err)) continue;
-                        uint8_t* base = smem + off;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            poison16(base + ((k ^ (r & 7)) << 4));
-                            *reinterpret_cast<uint4*>(base + ((k ^ (r & 7)) << 4)) =
-                                make_uint4(dq[32 * bb + 4 * k], dq[32 * bb + 4 * k + 1],
-                                           dq[32 * bb + 4 * k + 2], dq[32 * bb + 4 * k + 3]);
-                        }
-                    }
-                }
-                if (with_dq) fence_proxy_async_smem();   // each writer: its stores -> async proxy
-                mbar_arrive(bar(L::kBarDQStaged));
-            }
+            // dQ of this tile (kDefer: of the previous one, after this tile's P/dS)
+            if (!L::kDefer || it > 0) read_out_dq(L::kDefer ? it - 1 : it);
         }
+        if (L::kDefer && n_iter > 0) read_out_dq(n_iter - 1);
         // Epilogue: warps 0-3 store dV (staging tile = the dS buffer), warps 4-7
         // dK (staging tile = query stage 0, free once the reduction issuer has
         // seen its last reduction read it).  Both need every MMA done.
