@@ -77,7 +77,8 @@ struct BwdLayout {
     static constexpr int kBarDP = 13;      // dP^T done (split schedule; S^T alone on kBarSdp)
     static constexpr int kBarAccRead = 14; // kDefer: the tile's dV/dK MMAs have read P^T / dS^T
     static constexpr int kBarDQSFree = 15; // kDefer: the reduction has read the dQ staging tile
-    static constexpr int kNumBars = 16;
+    static constexpr int kBarDPRead = 16;  // kDefer: every compute warp has loaded all its dP^T
+    static constexpr int kNumBars = 17;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     static constexpr uint32_t kTmemCols = 512;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // q_empty: the MMAs' commit + the reduction issuer once the stage was read
             if (i == L::kBarQEmpty || i == L::kBarQEmpty + 1) cnt = L::kDefer ? 1 : 2;
             if (i == L::kBarP || i == L::kBarP + 1) cnt = 256;
-            if (i == L::kBarDQRead || i == L::kBarDQStaged) cnt = 256;
+            if (i == L::kBarDQRead || i == L::kBarDQStaged || i == L::kBarDPRead) cnt = 256;
             mbar_init(bar(i), cnt);
         }
         *abort_flag = 0;
@@ -307,6 +308,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // columns per step; P^T at 32c, dS^T at 32c + 16).
 #pragma unroll
                 for (int ph = 0; ph < 2; ++ph) {
+                    if (L::kDefer && ph == 1 && it + 1 < n_iter) {
+                        // the next tile's dP^T while this tile's second chunks are
+                        // worked on, once every compute warp has loaded its dP^T
+                        const int s1 = (it + 1) & 1;
+                        if (!(ok = mbar_wait(bar(L::kBarDPRead), it & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait(bar(L::kBarQFull + s1), ((it + 1) >> 1) & 1, abort_flag))) break;
+                        tc_fence_after();
+                        issue_dp(s1);
+                    }
                     if (!(ok = mbar_wait(bar(L::kBarP + ph), it & 1, abort_flag))) break;
                     tc_fence_after();
 #pragma unroll
@@ -325,17 +335,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_commit(bar(L::kBarQEmpty + s));
                 {
                     if (L::kDefer && it + 1 < n_iter) {
-                        // the next tile's dP^T at once (every compute warp read dP^T
-                        // before its arrival), its S^T once the dV/dK MMAs have read
-                        // P^T / dS^T out of the S^T columns
+                        // the next tile's S^T once the dV/dK MMAs have read P^T / dS^T
+                        // out of the S^T columns (its dP^T is already issued)
                         mma_commit(bar(L::kBarAccRead));
-                        const int s1 = (it + 1) & 1;
-                        if (!(ok = mbar_wait(bar(L::kBarQFull + s1), ((it + 1) >> 1) & 1, abort_flag))) break;
-                        tc_fence_after();
-                        issue_dp(s1);
                         if (!(ok = mbar_wait(bar(L::kBarAccRead), it & 1, abort_flag))) break;
                         tc_fence_after();
-                        issue_s(s1);
+                        issue_s((it + 1) & 1);
                         mma_commit(bar(L::kBarSdp));
                     }
                 }
@@ -492,6 +497,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tmem_ld32(tS + 32 * c, sv);
                     } else {
                         tmem_ld32x2(tS + 32 * c, sv, tDP + 32 * c, dv);
+                        if (L::kDefer && cc == 1) {
+                            // this warp's last dP^T chunk is in registers: the next
+                            // tile's dP^T may overwrite the columns
+                            tc_fence_before();
+                            mbar_arrive(bar(L::kBarDPRead));
+                        }
                     }
                     // -lse2 / -Delta of this chunk's query rows, four at a time, one
                     // group ahead of use (16-byte shared loads, every lane the same
