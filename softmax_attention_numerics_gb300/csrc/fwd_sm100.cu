@@ -36,6 +36,13 @@ struct BoolTag {
     static constexpr bool value = B;
 };
 
+// max(a, b, c) in one instruction (the three-input form of sm_100).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 using namespace sm100;
 
 constexpr int kFwdThreads = 320;
@@ -323,18 +330,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 uint32_t* xu = reinterpret_cast<uint32_t*>(x);
                 tmem_ld32x2(tS, xu, tS + 32, xu + 32);
                 tmem_ld64_nowait(tS + 64, xu + 64);
+                // At D = 64 with the three-input max (one instruction per pair), and
+                // two chains for the half on the critical path; both measured faster
+                // at D = 64 and slower at D = 128.
                 float mr = -INFINITY;
+                if constexpr (D == 64) {
 #pragma unroll
-                for (int c = 0; c < kTile / 2; ++c) mr = fmaxf(mr, x[c]);
+                    for (int c = 0; c < kTile / 2; c += 2) mr = fmax3(mr, x[c], x[c + 1]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kTile / 2; ++c) mr = fmaxf(mr, x[c]);
+                }
                 tmem_wait_ld_regs64(xu + 64);
                 if constexpr (D == 64) {
-                    // two chains for the half on the critical path (measured faster at
-                    // D = 64, slower at D = 128)
                     float mr1 = -INFINITY;
 #pragma unroll
-                    for (int c = kTile / 2; c < kTile; c += 2) {
-                        mr = fmaxf(mr, x[c]);
-                        mr1 = fmaxf(mr1, x[c + 1]);
+                    for (int c = kTile / 2; c < kTile; c += 4) {
+                        mr = fmax3(mr, x[c], x[c + 1]);
+                        mr1 = fmax3(mr1, x[c + 2], x[c + 3]);
                     }
                     mr = fmaxf(mr, mr1);
                 } else {
