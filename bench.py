@@ -283,10 +283,13 @@ def ncu_traffic(kernel_key, workload):
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    e = d.get(kernel_key)
-    if not e or e.get("source_hash") != source_hash() or e.get("workload") != workload:
-        return None
-    return e.get("bytes_per_launch_full")
+    entries = d.get(kernel_key) or []
+    if isinstance(entries, dict):
+        entries = [entries]
+    for e in entries:
+        if e.get("source_hash") == source_hash() and e.get("workload") == workload:
+            return e.get("bytes_per_launch_full")
+    return None
 
 
 # ---------------------------------------------------------------- reference arm

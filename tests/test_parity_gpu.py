@@ -160,10 +160,17 @@ def test_varlen_gqa():
 
 # ------------------------------------------------------------- long sequences (sampled)
 
+LONG = [(S, 128) for S in (16384, 65536, 131072)] + [(16384, 64), (131072, 64)]
+
+
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("S", [16384, 65536, 131072])
-def test_long_seq(S, causal):
-    case = W.long_seq(S, causal)
+@pytest.mark.parametrize("S,D", LONG, ids=["S%d_D%d" % c for c in LONG])
+def test_long_seq(S, D, causal):
+    """Sampled rows of out, lse and dq at the long lengths (the benchmark's
+    S = 131072 among them, at both head dims: hundreds of query tiles per key
+    tile, so every buffer rotation of the backward's pipeline is exercised),
+    and one head's full dK / dV at S = 16384."""
+    case = W.long_seq(S, causal, D=D)
     res = gpu_run(case)
     assert_finite(res)
     rows = W.sample_rows(1, 16, S, n=64)
@@ -174,7 +181,7 @@ def test_long_seq(S, causal):
     ii = [r[2] for r in rows]
     got = dict(out=res["out"][bi, ii, hi], lse=res["lse"][bi, hi, ii], dq=res["dq"][bi, ii, hi])
     compare(got, dict(out=out, lse=lse, dq=dq), names=("out", "lse", "dq"),
-            ctx="long S=%d causal=%s" % (S, causal))
+            ctx="long S=%d D=%d causal=%s" % (S, D, causal))
     if S == 16384:
         h = 5
         qh, kh, vh, dh = (to64(case[n][0, :, h]) for n in ("q", "k", "v", "do"))
@@ -184,7 +191,7 @@ def test_long_seq(S, causal):
         _, dk, dv = O._bwd_head(qh, kh, vh, P, dh, case["scale"])
         del P
         compare(dict(dk=res["dk"][0, :, h], dv=res["dv"][0, :, h]), dict(dk=dk, dv=dv),
-                names=("dk", "dv"), ctx="long S=%d dk/dv head %d" % (S, h))
+                names=("dk", "dv"), ctx="long S=%d D=%d dk/dv head %d" % (S, D, h))
 
 
 # ------------------------------------------------------------- edge cases
@@ -203,6 +210,7 @@ EDGE = [
     (1, 0, 64, 2, 1, 128, False, "none"),            # no queries
     (1, 1000, 1000, 16, 2, 128, True, "none"),       # GQA G=8: dK/dV summed over 8 q heads
     (1, 1000, 1000, 16, 2, 64, False, "none"),
+    (1, 1000, 1000, 16, 2, 64, True, "none"),        # causal GQA: key tiles with 1..8 query tiles per head
     (4, 130, 130, 32, 32, 64, False, "none"),        # many small (batch, head) problems
     (2, 257, 383, 8, 4, 128, False, "bool_rows"),    # ragged in both dimensions, per-row mask
     (1, 513, 513, 4, 1, 128, True, "additive_random"),  # causal + additive mask, G=4
