@@ -4,13 +4,13 @@
 // transpose_v_kernel into the caller's workspace as vt [B,Hkv,D,Sk_pad] (keys
 // contiguous; Sk_pad = Sk rounded up to 16, padding keys 0), one descale
 // factor per tensor, D = 128.  Both MMAs are tcgen05 kind::f8f6f4 with E4M3 A
-// and B, fp32 accumulate, both operands K-major in shared memory:
+// and B, fp32 accumulate, B K-major in shared memory:
 //     S_t  = Q_t K_j^T          A = Q tile [128 rows][128 bytes], B = K tile
-//     O_t += P^_t(j) V_j        A = P^ tile [128 rows][128 keys], B = V^T tile
+//     O_t += P^_t(j) V_j        A = P^ in TMEM [128 lanes][32 columns of 4 keys], B = V^T tile
 // The softmax is the 16-bit kernel's (FlyDSL PR #1033, "The fix": always
 // m_new = max(m_ref, m_tile), lazy threshold 8): x = s * scale * dq * dk *
-// log2 e, p = exp2(min(x - m_ref, 8)), P^ = E4M3(p) written to a swizzled
-// shared tile for the P V product.  The fp8 helper of the same PR instead
+// log2 e, p = exp2(min(x - m_ref, 8)), P^ = E4M3(p) written over the first
+// 32 columns of S_t for the P V product.  The fp8 helper of the same PR instead
 // rebases the running max down to a lower tile max with a bounded factor;
 // that keeps the top P of a tile exact in E4M3 but leaves earlier terms
 // under-weighted, which a V = ones check cannot see, so it is not used here.
@@ -19,9 +19,9 @@
 //
 // One CTA = two 128-row query tiles of one (b, q head):
 //   warps 0-3 softmax tile 0, 4-7 tile 1, 8 TMA producer, 9 TMEM + MMA issuer.
-// TMEM: S0 | S1 | O0 | O1 (128 fp32 columns each).
-// Shared: Q0 Q1 (16 KB each) | K / V^T ring (16 KB stages) | P^0 P^1 (16 KB
-// each) | barriers.  Every tile is one 128-byte-wide swizzle-128 block.
+// TMEM: S0 | S1 | O0 | O1 (128 fp32 columns each; P^_t over S_t's first 32).
+// Shared: Q0 Q1 (16 KB each) | K / V^T ring (16 KB stages) | barriers.  Every
+// tile is one 128-byte-wide swizzle-128 block.
 #include "sm100_ptx.cuh"
 
 namespace attn {
@@ -47,8 +47,7 @@ struct Fp8Layout {
     static constexpr int kStages = 6;
     static constexpr int kQ = 0;
     static constexpr int kKV = 2 * kTileBytes;
-    static constexpr int kP = kKV + kStages * kTileBytes;
-    static constexpr int kBar = kP + 2 * kTileBytes;
+    static constexpr int kBar = kKV + kStages * kTileBytes;
     static constexpr int kBarQ = 0;
     static constexpr int kBarKVFull = 1;
     static constexpr int kBarKVEmpty = kBarKVFull + kStages;
@@ -78,19 +77,42 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// A with P^ in TMEM (the TS form): [128 lanes][8 columns] = 32 E4M3 of K per row.
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 lanes x 8 consecutive TMEM columns from registers.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 // Two fp32 -> two E4M3 (round to nearest even, saturating to +-448), lo in the low byte.
-__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
-// Two E4M3 (low byte first) -> float2, exactly.
-__device__ __forceinline__ float2 unpack_e4m3x2(uint32_t v) {
-    uint32_t h2;
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-        : "=r"(h2) : "r"(v));
-    return __half22float2(*reinterpret_cast<__half2*>(&h2));
+// acc.x += the low E4M3 of v, acc.y += the high one: both widen exactly to f16
+// and the mixed-precision add of sm_100 takes the f16 operand as it is (one
+// fp32 rounding per add, the same sums as converting to fp32 first).
+__device__ __forceinline__ float2 add_e4m3x2(float2 acc, uint16_t v) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t.reg .b32 h2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h2, %2;\n\t"
+        "mov.b32 {lo, hi}, h2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\t"
+        "add.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y) : "h"(v));
+    return acc;
 }
 
 __global__ void __launch_bounds__(kF8Threads, 1)
@@ -194,12 +216,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     mma_ss_f8(tmem + colS[t], desc_add(qd, kk * 32), desc_add(kd, kk * 32), idesc, kk > 0);
             };
             auto issue_pv = [&](int t, int j) {
-                const uint64_t pd = smem_desc(sbase + L::kP + t * L::kTileBytes, 16, 1024, kSwizzle128B);
                 const uint64_t vd = smem_desc(sbase + L::kKV + kv_stage(2 * j + 1) * L::kTileBytes, 16,
                                               1024, kSwizzle128B);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)      // 32 keys per MMA
-                    mma_ss_f8(tmem + colO[t], desc_add(pd, kk * 32), desc_add(vd, kk * 32), idesc,
+                for (int kk = 0; kk < 4; ++kk)      // 32 keys (8 TMEM columns of P^) per MMA
+                    mma_ts_f8(tmem + colO[t], tmem + colS[t] + 8 * kk, desc_add(vd, kk * 32), idesc,
                               (j > 0 || kk > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(bar(L::kBarQ), 0, abort_flag);
@@ -231,7 +252,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     }
                     if (t == 1) mma_commit(bar(L::kBarKVEmpty + kv_stage(lv)));
                     if (j + 1 < n_t[t]) {
-                        // The softmax of S_t(j+1) rescales O_t and rewrites P^_t: PV_t(j) first.
+                        // S_t(j+1) overwrites P^_t(j), and its softmax rescales O_t: PV_t(j) first.
                         if (!(ok = mbar_wait(bar(L::kBarPVDone + t), j & 1, abort_flag))) break;
                         tc_fence_after();
                         issue_qk(t, j + 1);
@@ -256,7 +277,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + (t ? L::kColS1 : L::kColS0);
         const uint32_t tO = tmem + lane_off + (t ? L::kColO1 : L::kColO0);
-        uint8_t* prow = smem + L::kP + t * L::kTileBytes + r_local * 128;
+        const int r0_tile = m0 + t * kF8Tile;
         const int n_mine = n_t[t];
         float m_ref = -INFINITY;
         float2 l2 = make_float2(0.f, 0.f), lr2 = make_float2(0.f, 0.f);
@@ -270,15 +291,35 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             }
             tc_fence_after();
             const int n0 = j * kF8Tile;
+            // keys past the sequence or causal pairs in this tile: predicated path
+            const bool pred = (n0 + kF8Tile > p.Sk) || (p.causal && n0 + kF8Tile - 1 > r0_tile);
             float x[kF8Tile];
-            tmem_ld128(tS, reinterpret_cast<uint32_t*>(x));
-            const int jmax = p.causal ? min(p.Sk, i + 1) : p.Sk;
-            const bool row_in = i < p.Sq;
             float mt = -INFINITY;
+            uint32_t* xu = reinterpret_cast<uint32_t*>(x);
+            if (pred) {
+                tmem_ld128(tS, xu);
+                const int jmax = p.causal ? min(p.Sk, i + 1) : p.Sk;
+                const bool row_in = i < p.Sq;
 #pragma unroll
-            for (int c = 0; c < kF8Tile; ++c) {
-                x[c] = (row_in && n0 + c < jmax) ? x[c] * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, x[c]);
+                for (int c = 0; c < kF8Tile; ++c) {
+                    x[c] = (row_in && n0 + c < jmax) ? x[c] * p.scale_log2 : -INFINITY;
+                    mt = fmaxf(mt, x[c]);
+                }
+            } else {
+                // full tile: the max of the raw scores, scaled once (x stays
+                // unscaled; P folds the scale into one FMA).  The row loaded in two
+                // halves with the first half's max under the second load, as in the
+                // 16-bit kernel, spills here.
+                tmem_ld128(tS, xu);
+                float mr = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kF8Tile; ++c) mr = fmaxf(mr, x[c]);
+                if (p.scale_log2 > 0.f) {
+                    mt = mr * p.scale_log2;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kF8Tile; ++c) mt = fmaxf(mt, x[c] * p.scale_log2);
+                }
             }
             const float m_new = fmaxf(m_ref, mt);
             bool rescale = true;
@@ -292,37 +333,38 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 m_ref = m_new;
             }
             const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
-            // P^ row: 128 E4M3 = 8 chunks of 16 bytes, chunk c at (c ^ (row & 7)) * 16.
-            // p = exp2(min(x - m_ref, 8)); x - m_ref <= m_tile - m_ref exactly (x is
-            // the scaled score itself), so when every row of the warp has
-            // m_tile - m_ref <= 8 the per-element min is skipped.
+            const float2 nms2 = make_float2(-ms, -ms);
+            const float2 c2 = pred ? make_float2(1.f, 1.f) : make_float2(p.scale_log2, p.scale_log2);
+            // P^ row: 128 E4M3, four keys per TMEM column, over S_t's columns [0, 32).
+            // p = exp2(min(x - m_ref, 8)); x - m_ref <= m_tile - m_ref up to the
+            // rounding of the scaled maximum, so when every row of the warp has
+            // m_tile - m_ref <= 8 - 1/64 the per-element min is skipped.
             auto exps = [&](auto clamp_tag) {
                 constexpr bool kClamp = decltype(clamp_tag)::value;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t w[4];
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t w[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k0 = 16 * c + 4 * e;
-                        float pv[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            pv[u] = ex2(kClamp ? fminf(x[k0 + u] - ms, 8.f) : x[k0 + u] - ms);
-                        l2 = fadd2(l2, make_float2(pv[0] + pv[2], pv[1] + pv[3]));
-                        const uint32_t lo = pack_e4m3x2(pv[0], pv[1]), hi = pack_e4m3x2(pv[2], pv[3]);
-                        const float2 a = unpack_e4m3x2(lo), bq = unpack_e4m3x2(hi);
-                        lr2 = fadd2(lr2, make_float2(a.x + bq.x, a.y + bq.y));
-                        w[e] = lo | (hi << 16);
+                    for (int e = 0; e < 8; ++e) {
+                        const int k0 = 32 * c + 4 * e;
+                        const float2 d01 = ffma2(make_float2(x[k0], x[k0 + 1]), c2, nms2);
+                        const float2 d23 = ffma2(make_float2(x[k0 + 2], x[k0 + 3]), c2, nms2);
+                        const float2 p01 = make_float2(ex2(kClamp ? fminf(d01.x, 8.f) : d01.x),
+                                                       ex2(kClamp ? fminf(d01.y, 8.f) : d01.y));
+                        const float2 p23 = make_float2(ex2(kClamp ? fminf(d23.x, 8.f) : d23.x),
+                                                       ex2(kClamp ? fminf(d23.y, 8.f) : d23.y));
+                        l2 = fadd2(fadd2(l2, p01), p23);
+                        const uint16_t lo = pack_e4m3x2(p01.x, p01.y), hi = pack_e4m3x2(p23.x, p23.y);
+                        lr2 = add_e4m3x2(add_e4m3x2(lr2, lo), hi);
+                        w[e] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
                     }
-                    *reinterpret_cast<uint4*>(prow + ((c ^ (r_local & 7)) << 4)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                    tmem_st8(tS + 8 * c, w);
                 }
             };
-            if (__all_sync(0xffffffffu, mt - ms <= 8.f))
+            if (__all_sync(0xffffffffu, mt - ms <= 8.f - 0.015625f))
                 exps(F8Tag<false>{});
             else
                 exps(F8Tag<true>{});
-            fence_proxy_async_smem();   // generic stores of P^ -> tensor core reads
             if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
