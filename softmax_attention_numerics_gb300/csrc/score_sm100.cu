@@ -50,6 +50,7 @@ struct ScLayout {
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16 + 1024;     // + alignment slack
+    static_assert(kBytes <= 232448, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 256;
 };
 
@@ -209,15 +210,20 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const int jmax = p.causal ? min(si.len_k, i + 1) : si.len_k;   // keys < jmax visible
         const bool full = n0 + c0 + 64 <= jmax;              // every key of the half visible
         const float c = p.scale_log2;
-        const int64_t lse_row = b * p.lse_b + row_base + i;
+        // rows past the sequence read the last row's lse (a valid address) and
+        // discard it, so the load needs no predicate
+        const int64_t lse_row = b * p.lse_b + row_base + min(i, si.len_q - 1);
         float acc[64];
 #pragma unroll
         for (int e = 0; e < 64; ++e) acc[e] = 0.f;
         bool ok = true;
-        float nl_next = row_in ? -p.lse[lse_row] * kLog2e : 0.f;
+        // The next head's lse is loaded one head ahead and only converted when
+        // it is used: arithmetic on the value right after its load would wait
+        // for the load there, every head.
+        float lse_next = p.lse[lse_row];
         for (int h = 0; h < H; ++h) {
-            const float nl = nl_next;                        // -lse2 of (row, h)
-            if (h + 1 < H) nl_next = row_in ? -p.lse[lse_row + (h + 1) * p.lse_h] * kLog2e : 0.f;
+            const float lse_h = lse_next;
+            if (h + 1 < H) lse_next = p.lse[lse_row + (h + 1) * p.lse_h];
             const int buf = h & 1;
             ok = mbar_wait(bar(L::kBarSFull + buf), (h >> 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -229,6 +235,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
             tmem_ld32x2(tS + 128 * buf, v, tS + 128 * buf + 32, v + 32);
             tc_fence_before();
             mbar_arrive(bar(L::kBarSFree + buf));            // the values are in registers
+            const float nl = row_in ? -lse_h * kLog2e : 0.f;  // -lse2 of (row, h)
             if (full && row_in) {
                 // packed pairs: one FMA and one add per two terms
                 const float2 c2 = make_float2(c, c), nl2 = make_float2(nl, nl);
