@@ -65,9 +65,9 @@ struct SpLayout {
     static constexpr int kRingOff = 128 * kStRow;           // kRing x {Q, dO} x [64 heads][64 cols] bf16
     static constexpr int kDS = kRingOff + kRing * 16384;    // dS^T [128 entries][64 heads] bf16
     static constexpr int kBar = kDS + 16384;
-    static constexpr int kBarKV = 0;                        // gathered rows landed (64)
-    static constexpr int kBarRFull = 1, kBarREmpty = 1 + kRing;
-    static constexpr int kBarSdp = 1 + 2 * kRing;           // S^T and dP^T complete
+    static constexpr int kBarKV = 0;                        // [NB] a block of the gathered rows landed (64)
+    static constexpr int kBarRFull = NB, kBarREmpty = NB + kRing;
+    static constexpr int kBarSdp = NB + 2 * kRing;          // S^T and dP^T complete
     static constexpr int kBarPds = kBarSdp + 1;             // P^T, dS^T written (128)
     static constexpr int kBarKVFree = kBarPds + 1;          // gathered rows no longer read
     static constexpr int kBarDkvFull = kBarKVFree + 1;      // 2
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         for (int i = 0; i < L::kNumBars; ++i) {
             const bool by128 = i == L::kBarPds || i == L::kBarDkvFree || i == L::kBarDkvFree + 1 ||
                                i == L::kBarItemDone || i == L::kBarDQRead || i == L::kBarStageFree;
-            mbar_init(bar(i), i == L::kBarKV ? 64 : (by128 ? 128 : 1));
+            mbar_init(bar(i), i < L::kBarKV + NB ? 64 : (by128 ? 128 : 1));
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -220,15 +220,24 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                              16 * j;
                 }
                 const uint32_t dst = sbase + L::kKV + rs * 128 + ((j ^ rs) << 4);   // (8k + rs) & 7 = rs
+                // one copy group per 64-column block, each block signalled as it
+                // lands, so that the S^T / dP^T MMAs start on the first blocks
+                // while the later ones are still being copied
 #pragma unroll
-                for (int blk = 0; blk < NB; ++blk)
+                for (int blk = 0; blk < NB; ++blk) {
 #pragma unroll
                     for (int k = 0; k < kSpE / 8; ++k)
                         cp_async16(dst + blk * 16384 + k * 1024, src[k] + blk * 128);
-                cp_async_commit();
+                    cp_async_commit();
+                    if (blk > 0) {
+                        cp_async_wait(1);                    // this thread's part of block blk - 1
+                        fence_proxy_async_smem();            // generic-proxy writes -> UMMA reads
+                        mbar_arrive(bar(L::kBarKV + blk - 1));
+                    }
+                }
                 cp_async_wait(0);
-                fence_proxy_async_smem();                    // generic-proxy writes -> UMMA reads
-                mbar_arrive(bar(L::kBarKV));
+                fence_proxy_async_smem();
+                mbar_arrive(bar(L::kBarKV + NB - 1));
             }
         }
         cp_async_wait(0);
@@ -297,9 +306,10 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                     // previous item's dKV chunks have all been read out.
                     if (n > 0 && !(ok = mbar_wait(bar(L::kBarItemDone), (n - 1) & 1, abort_flag))) break;
                     tc_fence_after();
-                    // S^T and dP^T over the 64-column blocks of the gathered rows
-                    if (!(ok = mbar_wait(bar(L::kBarKV), n & 1, abort_flag))) break;
+                    // S^T and dP^T over the 64-column blocks of the gathered rows, each
+                    // once it has landed
                     for (int blk = 0; ok && blk < NB; ++blk) {
+                        if (!(ok = mbar_wait(bar(L::kBarKV + blk), n & 1, abort_flag))) break;
                         const uint64_t a = smem_desc(sbase + L::kKV + blk * 16384, 16, 1024, kSwizzle128B);
                         uint32_t ra;
                         const int s = ring_next(&ra);
