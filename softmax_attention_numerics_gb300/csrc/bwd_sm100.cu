@@ -26,6 +26,13 @@
 // chunks never wait on each other;
 // dQ_i = dS K then takes dP^T's columns as one N = D accumulator.
 // dV / dK MMAs for chunks 0 and 2 run while chunks 1 and 3 are computed.
+// D = 64 (TMEM has 128 spare columns, and the N = 64 dV / dK / dQ products
+// hold the tensor pipe for twice their math time): dQ_i has columns of its
+// own, dP^T(i+1) is issued once every compute warp has loaded its last dP^T
+// chunk, S^T(i+1) once the dV / dK MMAs have read P^T / dS^T, dQ_i after
+// them, and the compute warps read dQ_i out after tile i+1's P / dS into an
+// fp32 staging tile of its own (dS double-buffered), so dQ_i is off the
+// serial chain.
 //
 // Epilogue (PFCCLab/cudnn-frontend PR #9, section 1): every thread writes its
 // dK / dV row into a shared staging tile, fences its own writes for the async

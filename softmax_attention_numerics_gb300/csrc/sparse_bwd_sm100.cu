@@ -30,8 +30,9 @@
 //              limit); dq
 //   warps 4-5  gather the 128 selected kv rows with 16-byte cp.async (each
 //              warp instruction covers whole 128-byte row blocks) into the
-//              128-byte-swizzled operand layout (the rows stay resident for
-//              S^T, dP^T and dQ^T)
+//              128-byte-swizzled operand layout, one 64-column block at a
+//              time, each signalled on a barrier of its own as it lands (the
+//              rows stay resident for S^T, dP^T and dQ^T)
 //   warp 6     TMA: the 64 x 64 blocks of Q and dO of one 64-column slice
 //              together through a 3-stage ring (one wait and one release per
 //              slice), in the order the MMA issuer consumes them (twice per
