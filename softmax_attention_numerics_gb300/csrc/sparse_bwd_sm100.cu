@@ -63,6 +63,9 @@ struct SpLayout {
     // dKV staging over the same region during the dKV phase: 128 rows of half
     // a kv row in fp32 (NB x 128 bytes) + 16 bytes of padding (bank spread)
     static constexpr int kStRow = NB * 128 + 16;
+    // the staged pieces go out kGrp at a time (a third or a quarter of a half row)
+    static constexpr int kGrp = (NB % 3 == 0) ? 3 : 4;
+    static_assert(NB % kGrp == 0, "groups of whole pieces per half row");
     static constexpr int kRingOff = 128 * kStRow;           // kRing x {Q, dO} x [64 heads][64 cols] bf16
     static constexpr int kDS = kRingOff + kRing * 16384;    // dS^T [128 entries][64 heads] bf16
     static constexpr int kBar = kDS + 16384;
@@ -133,6 +136,11 @@ __device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int
 }
 __device__ __forceinline__ void bulk_wait_read_0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -484,15 +492,18 @@ __global__ void __launch_bounds__(kSpThreads, 1)
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
                             const int pc = 2 * j + half, q = pc % NB;
-                            if (pc == NB) bulk_wait_read_0();        // the first half row has been read
+                            // the group that read this slot in the first half row is done
+                            if (pc >= NB && pc % L::kGrp == 0) bulk_wait_read<NB / L::kGrp - 1>();
 #pragma unroll
                             for (int q4 = 0; q4 < 8; ++q4)
                                 sts128(st_row + 128 * q + 16 * q4, x[32 * half + 4 * q4],
                                        x[32 * half + 4 * q4 + 1], x[32 * half + 4 * q4 + 2],
                                        x[32 * half + 4 * q4 + 3]);
-                            if (q == NB - 1) {
+                            if (pc % L::kGrp == L::kGrp - 1) {
+                                // kGrp pieces (kGrp x 32 columns) complete: add them
+                                const int p0 = pc - (L::kGrp - 1);
                                 fence_proxy_async_smem();
-                                bulk_reduce_add_f32(acc_row + (pc / NB) * NB * 32, st_row, NB * 128);
+                                bulk_reduce_add_f32(acc_row + p0 * 32, st_row + 128 * (p0 % NB), L::kGrp * 128);
                                 bulk_commit();
                             }
                         }
