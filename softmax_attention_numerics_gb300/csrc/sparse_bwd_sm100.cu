@@ -63,9 +63,11 @@ struct SpLayout {
     // dKV staging over the same region during the dKV phase: 128 rows of half
     // a kv row in fp32 (NB x 128 bytes) + 16 bytes of padding (bank spread)
     static constexpr int kStRow = NB * 128 + 16;
-    // the staged pieces go out kGrp at a time (a third or a quarter of a half row)
-    static constexpr int kGrp = (NB % 3 == 0) ? 3 : 4;
-    static_assert(NB % kGrp == 0, "groups of whole pieces per half row");
+    // the staged pieces of a half row go out in two groups: pieces [0, kH1) and
+    // [kH1, NB) (5 + 4 at NB = 9, 4 + 4 at NB = 8)
+    static constexpr int kH1 = (NB + 1) / 2;
+    __device__ static constexpr int gfirst(int q) { return q < kH1 ? 0 : kH1; }
+    __device__ static constexpr bool glast(int q) { return q == kH1 - 1 || q == NB - 1; }
     static constexpr int kRingOff = 128 * kStRow;           // kRing x {Q, dO} x [64 heads][64 cols] bf16
     static constexpr int kDS = kRingOff + kRing * 16384;    // dS^T [128 entries][64 heads] bf16
     static constexpr int kBar = kDS + 16384;
@@ -493,17 +495,17 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                         for (int half = 0; half < 2; ++half) {
                             const int pc = 2 * j + half, q = pc % NB;
                             // the group that read this slot in the first half row is done
-                            if (pc >= NB && pc % L::kGrp == 0) bulk_wait_read<NB / L::kGrp - 1>();
+                            if (pc >= NB && L::gfirst(q) == q) bulk_wait_read<1>();
 #pragma unroll
                             for (int q4 = 0; q4 < 8; ++q4)
                                 sts128(st_row + 128 * q + 16 * q4, x[32 * half + 4 * q4],
                                        x[32 * half + 4 * q4 + 1], x[32 * half + 4 * q4 + 2],
                                        x[32 * half + 4 * q4 + 3]);
-                            if (pc % L::kGrp == L::kGrp - 1) {
-                                // kGrp pieces (kGrp x 32 columns) complete: add them
-                                const int p0 = pc - (L::kGrp - 1);
+                            if (L::glast(q)) {
+                                // a group of pieces (32 columns each) complete: add them
+                                const int q0 = L::gfirst(q), p0 = pc - (q - q0);
                                 fence_proxy_async_smem();
-                                bulk_reduce_add_f32(acc_row + p0 * 32, st_row + 128 * (p0 % NB), L::kGrp * 128);
+                                bulk_reduce_add_f32(acc_row + p0 * 32, st_row + 128 * q0, (q - q0 + 1) * 128);
                                 bulk_commit();
                             }
                         }
