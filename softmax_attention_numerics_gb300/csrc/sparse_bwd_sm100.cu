@@ -23,11 +23,13 @@
 //   dKV  [128 e x 64 d]  = dS^T . Q[:, d] + P^T . dO[:, d]   (A from TMEM)
 // Roles (256 threads, so that no register cap below 255 applies):
 //   warps 0-3  one entry per thread (TMEM lane): P^T, dS^T; the dKV rows,
-//              bulk-reduced (fp32 add) into the workspace row idx_e in two
-//              half-row operations, staged in the gathered-rows region once
-//              dQ^T no longer reads it (a few large bulk operations instead
-//              of many small ones: their count, not their bytes, is the
-//              limit); dq
+//              bulk-reduced (fp32 add) into the workspace row idx_e two
+//              operations per half row (pieces of 32 columns, 5 + 4 or
+//              4 + 4), staged in half-row slots of the gathered-rows region
+//              once dQ^T no longer reads it, each group's slots reused as soon
+//              as its add has read them (few large bulk operations: their
+//              count, not their bytes, is the limit, and adds that start
+//              early overlap the dKV MMAs); dq
 //   warps 4-5  gather the 128 selected kv rows with 16-byte cp.async (each
 //              warp instruction covers whole 128-byte row blocks) into the
 //              128-byte-swizzled operand layout, one 64-column block at a
